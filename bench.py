@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Benchmark: batched Nystrom decode throughput (group-steps/s) on GB300.
+
+Default workload ``batch64``: 64 sequences x 28 layers x 8 KV groups = 14336
+group states (heads_per_kv=2, d=dv=128, m=32, w=128, sink=4, Aggregate),
+sealed on a 256-token synthetic prompt, then decoded with one
+``nys_step_batch`` launch per token over all 14336 groups.  One benchmark
+step = one such token launch (all of the decode path: ring insert/evict, far
+insert, near and far read, rectifier, joint division).  The seal is timed once
+and reported beside it.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the same workload and metric instead.  Under torchrun each rank runs an
+independent replica of the workload on its own GPU (the states shard with no
+exchange), and ``value`` counts the group-steps of all ranks.
+"""
+from __future__ import annotations
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    __import__("os").environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("Nyström decode group-steps/s at batch 64, 28 layers; "
+          "achieved HBM GB/s vs peak")
+UNIT = "group-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+STEP_SOURCE = os.path.join(ROOT, "streaming_nystr_landmark_gb300", "csrc", "nys_step.cu")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "step_kernel_batch64.txt")
+
+
+def algorithmic_bytes(wl) -> int:
+    """Bytes one group-step must move at minimum (fp32): the window read, the
+    sinks, K~, the new k/v read and written into the ring; per head Q~, M,
+    T^ read and written, Z^ and m_max read and written, q and the output."""
+    f, H, m, w, s, d, dv = 4, wl.heads_per_kv, wl.m, wl.w, wl.sink, wl.d, wl.dv
+    shared = f * (w * (d + dv) + s * (d + dv) + m * d + 2 * (d + dv))
+    head = f * (m * d + m * m + 2 * m * dv + 4 * m + d + dv)
+    return shared + H * head
+
+
+def workload_config(wl, extra=None):
+    cfg = {
+        "workload": (f"{wl.name}: {wl.seqs} seq x {wl.layers} layers x "
+                     f"{wl.kv_groups} KV groups = {wl.n_groups} group states, "
+                     f"heads_per_kv={wl.heads_per_kv}, d={wl.d}, dv={wl.dv}, "
+                     f"m={wl.m}, w={wl.w}, sink={wl.sink}, "
+                     f"rect={'aggregate' if wl.rect == 0 else 'fm'}, "
+                     f"prompt t={wl.t}"),
+        "groups_per_launch": wl.n_groups,
+        "heads_per_kv": wl.heads_per_kv,
+        "prompt_len": wl.t,
+        "inputs": "synthetic fp32 N(0,1), k mean " + wl.k_mean,
+        "l2": ("state per launch far above the 126 MB L2 (no flush needed)"
+               if algorithmic_bytes(wl) * wl.n_groups > 512e6 else
+               "state fits in L2: latency-bound, roofline fraction not meaningful"),
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram read+write bytes per launch of the step kernel from the committed
+    ncu summary, or None when that summary was taken on another version of
+    the kernel source."""
+    try:
+        src = hashlib.sha256(open(STEP_SOURCE, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for line in open(TRAFFIC_PROFILE):
+            if ":" in line:
+                key, val = line.split(":", 1)
+                fields[key.strip()] = val.strip()
+        if fields.get("step_source_sha256_16") != src:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="nys_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        reasons = sorted({n for r in rows for n, val in zip(names, r[5:9])
+                          if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ dist
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle
+def time_oracle(wl, groups, steps, warmup=0, budget_s=None):
+    """Seal `groups` with the fp64 oracle (untimed), then time decode tokens
+    round-robin over them.  Returns (group_steps, seconds, tokens_timed)."""
+    from oracle import NystromOracle
+    from streaming_nystr_landmark_gb300.workloads import GroupInputs
+    states = []
+    for g in groups:
+        gi = GroupInputs(wl, g)
+        q, k, v = gi.prompt()
+        o = NystromOracle(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.rect)
+        o.prefill(q, k, v)
+        states.append((o, gi))
+    n = 0
+    for _ in range(warmup):
+        for o, gi in states:
+            o.step(*gi.token(n))
+        n += 1
+    t0 = time.perf_counter()
+    done = 0
+    while done < steps:
+        for o, gi in states:
+            o.step(*gi.token(n))
+        n += 1
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done * len(groups), dt, done
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    groups = [0, wl.n_groups // 3, wl.n_groups - 1][: max(1, args.ref_groups)]
+    gs, dt, done = time_oracle(wl, groups, args.steps, args.warmup)
+    value = gs / dt
+    sample = (f"{len(groups)} of {wl.n_groups} groups, sealed untimed on the "
+              f"t={wl.t} prompt, then {args.warmup} untimed + {done} timed "
+              f"decode tokens each; fp64 numpy oracle (streaming form), 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": done, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / max(done, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl, {"sampled_groups": len(groups)}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, wl):
+    import torch
+    from streaming_nystr_landmark_gb300.nys import NystromStates
+    from streaming_nystr_landmark_gb300.workloads import DeviceFill
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    G, H = wl.n_groups, wl.heads_per_kv
+    st = NystromStates(wl.m, wl.w, wl.sink, H, wl.d, wl.dv, G, wl.rect, dev)
+    fill = DeviceFill(wl, dev, seed=1000 + rank)
+
+    # ---- seal (timed once)
+    q = torch.empty((G, H, wl.t, wl.d), device=dev)
+    k = torch.empty((G, wl.t, wl.d), device=dev)
+    v = torch.empty((G, wl.t, wl.dv), device=dev)
+    fill.prompt_into(q, k, v)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s0.record()
+    st.seal(q, k, v)
+    s1.record()
+    torch.cuda.synchronize(dev)
+    seal_ms = s0.elapsed_time(s1)
+    del q, k, v
+    torch.cuda.empty_cache()
+
+    # ---- decode inputs resident in HBM before timing
+    total = args.warmup + args.steps
+    pool = min(total, args.pool)
+    tq = torch.empty((pool, G, H, wl.d), device=dev)
+    tk = torch.empty((pool, G, wl.d), device=dev)
+    tv = torch.empty((pool, G, wl.dv), device=dev)
+    chunk = 64
+    for c0 in range(0, pool, chunk):
+        c1 = min(pool, c0 + chunk)
+        fill.tokens_into(tq[c0:c1], tk[c0:c1], tv[c0:c1])
+    out = torch.empty((G, H, wl.dv), device=dev)
+    step_i = 0
+    for _ in range(args.warmup):
+        j = step_i % pool
+        st.step(tq[j], tk[j], tv[j], out)
+        step_i += 1
+    torch.cuda.synchronize(dev)
+    barrier(world)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0.record()
+    for _ in range(args.steps):
+        j = step_i % pool
+        st.step(tq[j], tk[j], tv[j], out)
+        step_i += 1
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    dt = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    value = world * G * args.steps / dt
+    launch_s = dt / args.steps
+    finite = bool(torch.isfinite(out).all().item())
+    del tq, tk, tv
+
+    # ---- end to end through pinned host buffers
+    pe = 4
+    hq = [torch.empty((G, H, wl.d), pin_memory=True) for _ in range(pe)]
+    hk = [torch.empty((G, wl.d), pin_memory=True) for _ in range(pe)]
+    hv = [torch.empty((G, wl.dv), pin_memory=True) for _ in range(pe)]
+    for i in range(pe):
+        hq[i].normal_()
+        hk[i].normal_()
+        hv[i].normal_()
+    hout = torch.empty((G, H, wl.dv), pin_memory=True)
+    dq = torch.empty((G, H, wl.d), device=dev)
+    dk = torch.empty((G, wl.d), device=dev)
+    dvv = torch.empty((G, wl.dv), device=dev)
+    e2e_steps = args.steps
+    for i in range(2):
+        st.step_host(hq[i], hk[i], hv[i], hout, dq, dk, dvv, out)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record()
+    for i in range(e2e_steps):
+        st.step_host(hq[i % pe], hk[i % pe], hv[i % pe], hout, dq, dk, dvv, out)
+    e3.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    dt_e2e = max_over_ranks(e2.elapsed_time(e3) / 1e3, world, dev)
+    e2e = {"value": world * G * e2e_steps / dt_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": 4 * G * (H * wl.d + wl.d + wl.dv),
+           "d2h_bytes_per_step": 4 * G * H * wl.dv}
+    st.close()
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    per_launch = algorithmic_bytes(wl) * G
+    achieved = per_launch / launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(),
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": per_launch,
+                "kernel": "step_kernel<2> (one launch per token)"}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        groups = [0, G // 2, G - 1]
+        gs, cdt, done = time_oracle(wl, groups, 10 ** 9, budget_s=args.cpu_budget)
+        cpu = {"value": gs / cdt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": (f"{len(groups)} of {G} groups sealed untimed, then "
+                          f"{done} decode tokens each in {cdt:.1f} s; fp64 numpy "
+                          "oracle (streaming form), 1 thread")}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(wl, {"parallelism": f"replicas x{world}",
+                                       "seal_ms": seal_ms,
+                                       "decode_input_pool": pool,
+                                       "outputs_finite": finite}),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="batch64")
+    ap.add_argument("--pool", type=int, default=256,
+                    help="distinct decode-token batches kept in HBM (cycled)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-groups", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from streaming_nystr_landmark_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * nys.h -- C ABI of libnys: batched streaming Nystrom (landmark) attention
+ * for GQA decode on one NVIDIA GB300 (sm_103a).
+ *
+ * The operator is the one defined in the module documentation of
+ * cortiq_engine's nystrom.rs (docs.rs source view, cortiq-engine 0.5.71):
+ *
+ *   out(q) = (sum_near e_j v_j + F M T_far) / (sum_near e_j + F M Z_far)
+ *   e_j = exp(q.k_j/sqrt(d)),  F_a = exp(q.k~_a/sqrt(d)),
+ *   M = pinv_reg(exp(Q~ K~^T/sqrt(d))),
+ *   T_far = sum_far exp(Q~ k_j/sqrt(d)) v_j^T,  Z_far = sum_far exp(Q~ k_j/sqrt(d)),
+ *
+ * with an exact ring window of the last w keys, `sink` permanent exact keys,
+ * delayed insertion of a key into the far field at the step it leaves the
+ * window, per-landmark running maxima, and one joint division.
+ *
+ * Conventions for every entry point:
+ *  - Return 0 (NYS_OK) on success, a negative nys_status otherwise.  The
+ *    library never aborts, never traps the GPU and never prints except the
+ *    one-time landmark-clamp notice described at nys_seal.
+ *  - Every float pointer is a DEVICE pointer to fp32, row-major, 16-byte
+ *    aligned, owned by the caller; the library reads inputs and writes only
+ *    `out` and the state buffer.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it.  Host-side validation
+ *    happens before anything is enqueued, so an error return means nothing
+ *    was launched (except NYS_E_CUDA, which reports a failed launch).
+ *  - A "group" is one (sequence, layer, KV head) state: the shared window,
+ *    sinks and key landmarks plus heads_per_kv private query-head parts.
+ *    Query head h of group g is global head g*heads_per_kv + h, so a group's
+ *    heads are contiguous in q and out (Struct LayerKvCache, o1_step).
+ */
+#ifndef NYS_H
+#define NYS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NYS_OK = 0,
+  NYS_E_INVAL = -1,      /* bad geometry (m<4, w<1, heads<1, sink<0, d or dv
+                            not a positive multiple of 4, unknown rect) or a
+                            NULL argument                                      */
+  NYS_E_RANGE = -2,      /* group range outside the handle, or t <= sink      */
+  NYS_E_NOT_SEALED = -3, /* decode step on a group that was never sealed      */
+  NYS_E_EXACT_ONLY = -4, /* prompt t <= w + sink + 8: short-prompt mode, which
+                            this GPU path does not carry                       */
+  NYS_E_BUF = -5,        /* caller buffer smaller than nys_memory_bytes       */
+  NYS_E_ALIGN = -6,      /* pointer not 16-byte aligned (state: 256-byte)     */
+  NYS_E_CUDA = -7,       /* a CUDA call or kernel launch failed               */
+  NYS_E_UNSUPPORTED = -8 /* geometry beyond the kernels' limits: m > 64,
+                            d or dv > 256, heads_per_kv > 64, sink + w > 2048  */
+} nys_status;
+
+/* Rectifier of the skeleton's far mass (nystrom.rs, enum O1Rect).
+ * AGGREGATE, the default (nystrom.rs, O1_DEFAULT_RECT): a row whose far
+ * denominator is negative drops its far field.  FM: clamp u = F^ M at 0. */
+typedef enum { NYS_RECT_AGGREGATE = 0, NYS_RECT_FM = 1 } nys_rect;
+
+/* Geometry shared by every group of a handle (nystrom.rs,
+ * NystromState::new_group(m, w, sink, q_heads) and with_rect; the page fixes
+ * d and dv at seal time, this library at allocation, so that the state can
+ * be laid out up front). */
+typedef struct {
+  int32_t m;            /* landmark budget, >= 4 (page default 32)            */
+  int32_t w;            /* exact window width, >= 1 (page default 128)        */
+  int32_t sink;         /* permanent exact sink keys, >= 0 (page default 4)   */
+  int32_t heads_per_kv; /* query heads per group, >= 1                        */
+  int32_t d;            /* query/key head dim, positive multiple of 4         */
+  int32_t dv;           /* value head dim, positive multiple of 4             */
+  int32_t rect;         /* nys_rect                                           */
+} nys_config;
+
+typedef struct nys_states nys_states; /* opaque host handle */
+
+/* Device layout of the state buffer: the analogue of nystrom.rs
+ * O1DeviceView / O1HeadView (every slice the device mirror needs, in the
+ * layout the kernels index).  Offsets are bytes from the buffer base; every
+ * region starts on a 256-byte boundary and is indexed [group][...] as below.
+ * Storage is strided by the budget m: a group sealed with m_eff < m uses the
+ * leading m_eff rows, and the top-left m_eff x m_eff block of mu (row
+ * stride m).
+ *
+ *   win_k   f32 [G][w][d]        ring window keys   (shared per group)
+ *   win_v   f32 [G][w][dv]       ring window values
+ *   sink_k  f32 [G][sink][d]     sink keys
+ *   sink_v  f32 [G][sink][dv]    sink values
+ *   k_tilde f32 [G][m][d]        key landmarks K~
+ *   q_tilde f32 [G][H][m][d]     query landmarks Q~ (per head)
+ *   mu      f32 [G][H][m][m]     M: row = key landmark a, column = query
+ *                                landmark b
+ *   t_hat   f32 [G][H][m][dv]    far numerator at scale e^{-m_max}
+ *   z_hat   f32 [G][H][m]        far denominator, same scale
+ *   m_max   f32 [G][H][m]        per-landmark running max of far logits
+ *   far_len i32 [G][H]           keys absorbed per head
+ *   ints    i32 [G][8]           {win_head, win_len, m_eff, t, mode, 0, 0, 0},
+ *                                mode 0 = empty, 1 = sealed (landmark path)
+ */
+typedef struct {
+  size_t total_bytes;
+  size_t off_win_k, off_win_v, off_sink_k, off_sink_v, off_k_tilde;
+  size_t off_q_tilde, off_mu, off_t_hat, off_z_hat, off_m_max;
+  size_t off_far_len, off_ints;
+  int64_t n_groups;
+  int32_t ints_per_group; /* 8 */
+} nys_layout;
+
+/* Host-visible summary of one group (nystrom.rs, NystromState::far_len and
+ * the O1DeviceView scalars). */
+typedef struct {
+  int32_t mode;     /* 0 empty, 1 sealed                                      */
+  int32_t m_eff;    /* effective landmark count, clamp(t/8, 4, m)             */
+  int32_t t;        /* prompt length the group was sealed with                */
+  int32_t win_len;  /* keys in the window (w once sealed)                     */
+  int32_t win_head; /* ring slot of the oldest window key                     */
+} nys_group_info;
+
+/* Bytes of device memory a handle of n_groups groups needs (nystrom.rs,
+ * NystromState::memory_bytes: window, sinks and K~ once per group; far field,
+ * Q~ and M per head.  The page's per-head score scratch is not carried: the
+ * kernels keep it on chip).  Writes *device_bytes.  Host arithmetic only;
+ * needs no GPU.  Errors: NYS_E_INVAL, NYS_E_UNSUPPORTED. */
+int nys_memory_bytes(const nys_config* cfg, int64_t n_groups,
+                     size_t* device_bytes);
+
+/* Create a handle for n_groups groups (nystrom.rs, NystromState::new_group,
+ * once per group).  dev_buf == NULL: the library cudaMallocs
+ * nys_memory_bytes bytes and frees them in nys_free_states.  Otherwise
+ * dev_buf is a caller-owned device buffer of at least that size (e.g. a torch
+ * tensor), 256-byte aligned, which must outlive the handle.  The buffer is
+ * zeroed synchronously, so every group starts empty.  *out receives the
+ * handle.  Errors: NYS_E_INVAL, NYS_E_UNSUPPORTED, NYS_E_BUF, NYS_E_ALIGN,
+ * NYS_E_CUDA. */
+int nys_alloc_states(const nys_config* cfg, int64_t n_groups, void* dev_buf,
+                     size_t buf_bytes, nys_states** out);
+
+/* Destroy a handle, and the buffer if the library allocated it.  The caller
+ * must make sure no enqueued work still uses it.  NULL is a no-op. */
+int nys_free_states(nys_states* st);
+
+/* Seal groups [g0, g0+n) on a prompt of t positions (nystrom.rs,
+ * NystromState::prefill_group, prefill_shared, NystromHead::seal,
+ * seg_means, ridge_pinv, cholesky; Struct NystromState, prefill_group):
+ *  - sinks = keys/values 0..sink; m_eff = clamp(t/8, 4, m), with one notice
+ *    on stderr per process when m_eff < m, as the page warns once;
+ *  - K~ = segment means of the keys, Q~_h = segment means of head h's
+ *    queries (f64 accumulation, stored f32);
+ *  - M_h = (A^T A + lambda I)^-1 A^T of A = exp(Q~ K~^T / sqrt(d)) in f64,
+ *    lambda = 1e-6 * mean diag(A^T A), tenfold growth after a failed
+ *    Cholesky, at most twelve attempts, stored f32;
+ *  - positions sink..t-1 replayed through the window: the last w sit in the
+ *    ring, keys sink..t-w-1 are in every head's far field with per-landmark
+ *    running max, far_len = t - sink - w.
+ * Inputs: q [n][heads_per_kv][t][d], k [n][t][d], v [n][t][dv] (device).
+ * All n groups share t.  Re-sealing a group replaces its state.  Allocates a
+ * temporary f64 workspace of n*m*d*8 bytes with cudaMallocAsync on `stream`
+ * and frees it there.  Writes no attention output (the page's prefill
+ * writes none).
+ * Errors: NYS_E_INVAL, NYS_E_RANGE, NYS_E_EXACT_ONLY, NYS_E_ALIGN,
+ * NYS_E_CUDA. */
+int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t,
+             const float* q, const float* k, const float* v, void* stream);
+
+/* One decode token for groups [g0, g0+n) (nystrom.rs,
+ * NystromState::step_group and advance, NystromHead::step and far_insert;
+ * Struct NystromState, step_group): insert each group's (k, v) once -- a full
+ * ring first evicts its oldest key into every head's far field -- then write
+ * every head's output.
+ * Inputs: q [n][heads_per_kv][d], k [n][d], v [n][dv]; output
+ * out [n][heads_per_kv][dv] (all device).  One kernel launch.
+ * Errors: NYS_E_INVAL, NYS_E_RANGE, NYS_E_NOT_SEALED, NYS_E_ALIGN,
+ * NYS_E_CUDA. */
+int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
+                   const float* k, const float* v, float* out, void* stream);
+
+/* Read one group's counters to the host (nystrom.rs, NystromState::far_len,
+ * and the O1DeviceView scalars).  far_len, if not NULL, receives
+ * heads_per_kv entries.  Synchronises `stream`.  Errors: NYS_E_INVAL,
+ * NYS_E_RANGE, NYS_E_CUDA. */
+int nys_query(const nys_states* st, int64_t g, nys_group_info* info,
+              int32_t* far_len, void* stream);
+
+/* The state buffer's base pointer and layout (see nys_layout), so that a
+ * caller can read or write any group's state in place, as the page's
+ * device_view exposes a sealed group for upload.  Errors: NYS_E_INVAL. */
+int nys_layout_of(const nys_states* st, void** base, nys_layout* layout);
+
+/* Declare groups [g0, g0+n) sealed after the caller wrote a complete sealed
+ * state into them through nys_layout_of (their ints.mode must be 1 and their
+ * ring full).  Host bookkeeping only; nothing is launched.
+ * Errors: NYS_E_INVAL, NYS_E_RANGE. */
+int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n);
+
+/* The geometry a handle was created with.  Errors: NYS_E_INVAL. */
+int nys_config_of(const nys_states* st, nys_config* cfg, int64_t* n_groups);
+
+/* Static description of a status code.  Never NULL. */
+const char* nys_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NYS_H */

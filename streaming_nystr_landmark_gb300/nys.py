@@ -1,0 +1,271 @@
+"""ctypes binding of libnys (include/nys.h): same names, argument marshalling only.
+
+Every operation runs in the CUDA kernels of libnys.so.  Importing this module
+raises ImportError if the library has not been built, and every call raises
+NysError on a non-zero status: there is no fallback.
+
+``NystromStates`` is a convenience wrapper that keeps the state buffer in a
+torch tensor and passes torch tensors' device pointers and the current torch
+stream to the C calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnys.so")
+
+NYS_OK = 0
+NYS_E_INVAL = -1
+NYS_E_RANGE = -2
+NYS_E_NOT_SEALED = -3
+NYS_E_EXACT_ONLY = -4
+NYS_E_BUF = -5
+NYS_E_ALIGN = -6
+NYS_E_CUDA = -7
+NYS_E_UNSUPPORTED = -8
+NYS_RECT_AGGREGATE = 0
+NYS_RECT_FM = 1
+
+# Every entry point include/nys.h declares.
+EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
+            "nys_seal", "nys_step_batch", "nys_query", "nys_layout_of",
+            "nys_mark_sealed", "nys_config_of", "nys_strerror")
+
+
+class NysConfig(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("w", ctypes.c_int32),
+                ("sink", ctypes.c_int32), ("heads_per_kv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("rect", ctypes.c_int32)]
+
+
+class NysLayout(ctypes.Structure):
+    _fields_ = [("total_bytes", ctypes.c_size_t),
+                ("off_win_k", ctypes.c_size_t), ("off_win_v", ctypes.c_size_t),
+                ("off_sink_k", ctypes.c_size_t), ("off_sink_v", ctypes.c_size_t),
+                ("off_k_tilde", ctypes.c_size_t), ("off_q_tilde", ctypes.c_size_t),
+                ("off_mu", ctypes.c_size_t), ("off_t_hat", ctypes.c_size_t),
+                ("off_z_hat", ctypes.c_size_t), ("off_m_max", ctypes.c_size_t),
+                ("off_far_len", ctypes.c_size_t), ("off_ints", ctypes.c_size_t),
+                ("n_groups", ctypes.c_int64), ("ints_per_group", ctypes.c_int32)]
+
+
+class NysGroupInfo(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("m_eff", ctypes.c_int32),
+                ("t", ctypes.c_int32), ("win_len", ctypes.c_int32),
+                ("win_head", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -m streaming_nystr_landmark_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I64, I32, VP = ctypes.POINTER, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    sig = {
+        "nys_memory_bytes": [P(NysConfig), I64, P(ctypes.c_size_t)],
+        "nys_alloc_states": [P(NysConfig), I64, VP, ctypes.c_size_t, P(VP)],
+        "nys_free_states": [VP],
+        "nys_seal": [VP, I64, I64, I32, VP, VP, VP, VP],
+        "nys_step_batch": [VP, I64, I64, VP, VP, VP, VP, VP],
+        "nys_query": [VP, I64, P(NysGroupInfo), P(I32), VP],
+        "nys_layout_of": [VP, P(VP), P(NysLayout)],
+        "nys_mark_sealed": [VP, I64, I64],
+        "nys_config_of": [VP, P(NysConfig), P(I64)],
+        "nys_strerror": [ctypes.c_int],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "nys_strerror" else ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+class NysError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {nys_strerror(code)} (status {code})")
+
+
+def _check(code: int, where: str):
+    if code != NYS_OK:
+        raise NysError(code, where)
+
+
+def nys_strerror(code: int) -> str:
+    return _lib.nys_strerror(code).decode()
+
+
+def make_config(m, w, sink, heads_per_kv, d, dv, rect=NYS_RECT_AGGREGATE) -> NysConfig:
+    return NysConfig(m, w, sink, heads_per_kv, d, dv, rect)
+
+
+def nys_memory_bytes(cfg: NysConfig, n_groups: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.nys_memory_bytes(ctypes.byref(cfg), n_groups, ctypes.byref(out)),
+           "nys_memory_bytes")
+    return out.value
+
+
+def nys_alloc_states(cfg: NysConfig, n_groups: int, dev_buf: int = 0,
+                     buf_bytes: int = 0) -> int:
+    h = ctypes.c_void_p(0)
+    _check(_lib.nys_alloc_states(ctypes.byref(cfg), n_groups, dev_buf or None,
+                                 buf_bytes, ctypes.byref(h)), "nys_alloc_states")
+    return h.value
+
+
+def nys_free_states(handle: int):
+    _check(_lib.nys_free_states(handle), "nys_free_states")
+
+
+def nys_seal(handle, g0, n, t, q, k, v, stream=0):
+    _check(_lib.nys_seal(handle, g0, n, t, q, k, v, stream or None), "nys_seal")
+
+
+def nys_step_batch(handle, g0, n, q, k, v, out, stream=0):
+    _check(_lib.nys_step_batch(handle, g0, n, q, k, v, out, stream or None),
+           "nys_step_batch")
+
+
+def nys_query(handle, g, heads, stream=0):
+    info = NysGroupInfo()
+    far = (ctypes.c_int32 * heads)()
+    _check(_lib.nys_query(handle, g, ctypes.byref(info), far, stream or None),
+           "nys_query")
+    return ({"mode": info.mode, "m_eff": info.m_eff, "t": info.t,
+             "win_len": info.win_len, "win_head": info.win_head}, list(far))
+
+
+def nys_layout_of(handle):
+    base = ctypes.c_void_p(0)
+    lay = NysLayout()
+    _check(_lib.nys_layout_of(handle, ctypes.byref(base), ctypes.byref(lay)),
+           "nys_layout_of")
+    return base.value, lay
+
+
+def nys_mark_sealed(handle, g0, n):
+    _check(_lib.nys_mark_sealed(handle, g0, n), "nys_mark_sealed")
+
+
+def nys_config_of(handle):
+    cfg = NysConfig()
+    n = ctypes.c_int64(0)
+    _check(_lib.nys_config_of(handle, ctypes.byref(cfg), ctypes.byref(n)),
+           "nys_config_of")
+    return cfg, n.value
+
+
+# ---------------------------------------------------------------- torch wrapper
+def _ptr(t, dtype, shape, where):
+    import torch
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{where}: need a contiguous CUDA {dtype} tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{where}: shape {tuple(t.shape)} != {tuple(shape)}")
+    return t.data_ptr()
+
+
+class NystromStates:
+    """A batch of group states in one torch-owned device buffer."""
+
+    def __init__(self, m, w, sink, heads_per_kv, d, dv, n_groups,
+                 rect=NYS_RECT_AGGREGATE, device="cuda"):
+        import torch
+        self.torch = torch
+        self.cfg = make_config(m, w, sink, heads_per_kv, d, dv, rect)
+        self.n_groups = n_groups
+        self.device = torch.device(device)
+        nbytes = nys_memory_bytes(self.cfg, n_groups)
+        self.buf = torch.empty(max(nbytes, 1) + 256, dtype=torch.uint8,
+                               device=self.device)
+        base = self.buf.data_ptr()
+        self._off = (-base) % 256
+        self.handle = nys_alloc_states(self.cfg, n_groups, base + self._off, nbytes)
+        self.base, self.layout = nys_layout_of(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            nys_free_states(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def seal(self, q, k, v, g0=0, n=None):
+        c = self.cfg
+        n = k.shape[0] if n is None else n
+        t = k.shape[1]
+        torch = self.torch
+        nys_seal(self.handle, g0, n, t,
+                 _ptr(q, torch.float32, (n, c.heads_per_kv, t, c.d), "q"),
+                 _ptr(k, torch.float32, (n, t, c.d), "k"),
+                 _ptr(v, torch.float32, (n, t, c.dv), "v"), self._stream())
+
+    def step(self, q, k, v, out, g0=0, n=None):
+        c = self.cfg
+        n = k.shape[0] if n is None else n
+        torch = self.torch
+        nys_step_batch(self.handle, g0, n,
+                       _ptr(q, torch.float32, (n, c.heads_per_kv, c.d), "q"),
+                       _ptr(k, torch.float32, (n, c.d), "k"),
+                       _ptr(v, torch.float32, (n, c.dv), "v"),
+                       _ptr(out, torch.float32, (n, c.heads_per_kv, c.dv), "out"),
+                       self._stream())
+        return out
+
+    def step_host(self, hq, hk, hv, hout, dq, dk, dv, dout):
+        """One token from pinned host buffers: copy q/k/v to the device
+        staging tensors, launch nys_step_batch, copy the outputs back to
+        ``hout``; everything is enqueued on the current stream."""
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        self.step(dq, dk, dv, dout)
+        hout.copy_(dout, non_blocking=True)
+        return hout
+
+    def query(self, g):
+        return nys_query(self.handle, g, self.cfg.heads_per_kv, self._stream())
+
+    def region(self, name):
+        """A torch view of one state region, shaped as nys_layout documents."""
+        torch = self.torch
+        c, G = self.cfg, self.n_groups
+        H, m = c.heads_per_kv, c.m
+        shapes = {
+            "win_k": (torch.float32, (G, c.w, c.d)),
+            "win_v": (torch.float32, (G, c.w, c.dv)),
+            "sink_k": (torch.float32, (G, c.sink, c.d)),
+            "sink_v": (torch.float32, (G, c.sink, c.dv)),
+            "k_tilde": (torch.float32, (G, m, c.d)),
+            "q_tilde": (torch.float32, (G, H, m, c.d)),
+            "mu": (torch.float32, (G, H, m, m)),
+            "t_hat": (torch.float32, (G, H, m, c.dv)),
+            "z_hat": (torch.float32, (G, H, m)),
+            "m_max": (torch.float32, (G, H, m)),
+            "far_len": (torch.int32, (G, H)),
+            "ints": (torch.int32, (G, self.layout.ints_per_group)),
+        }
+        dtype, shape = shapes[name]
+        off = getattr(self.layout, "off_" + name) + self._off
+        count = 1
+        for s in shape:
+            count *= s
+        raw = self.buf[off: off + 4 * count]
+        return raw.view(dtype).view(shape)
+
+    def mark_sealed(self, g0=0, n=None):
+        nys_mark_sealed(self.handle, g0, self.n_groups if n is None else n)

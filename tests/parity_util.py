@@ -1,0 +1,183 @@
+"""Drive the CUDA path and the fp64 oracle side by side on the same inputs.
+
+The library runs every group of a workload in one launch per token.  Groups
+listed in ``sample`` receive host-drawn inputs from the seeded per-group
+streams, which the oracle also consumes; any other group receives
+device-drawn filler of the same distribution, so full-size launches stay full
+size while the oracle only runs the sampled groups.
+
+Tolerances (derived from fp32 evaluation of the step):
+  outputs         row-normwise  max|o - o_ref| / max|o_ref| <= 1e-4, except
+                  rows where the Aggregate guard sits within 1e-5 of its
+                  threshold (either branch is then correct) or where the far
+                  maxima sit > 80 above the near maximum (fp32 near weights
+                  underflow by design of the joint shift);
+  K~, Q~          <= 1e-6 relative to the row's max magnitude;
+  M               <= 1e-5 normwise relative;
+  T^, Z^, m_max   <= 1e-5, compared at a common scale;
+  window, sinks   bit-exact (copies of the inputs);
+  counters        bit-exact (far_len per head, win_head, win_len, m_eff, t).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import NystromOracle
+from streaming_nystr_landmark_gb300.workloads import (DeviceFill, GroupInputs,
+                                                      host_prompt_batch,
+                                                      host_token_batch)
+
+OUT_TOL = 1e-4
+LANDMARK_TOL = 1e-6
+MU_TOL = 1e-5
+FAR_TOL = 1e-5
+GUARD_BAND = 1e-5
+UNDERFLOW_GAP = 80.0
+
+
+def row_err(got, ref):
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+class ParityRun:
+    def __init__(self, wl, sample, device, n_groups=None, host_all=None):
+        import torch
+        from streaming_nystr_landmark_gb300.nys import NystromStates
+        self.torch = torch
+        self.wl = wl
+        self.dev = device
+        self.G = wl.n_groups if n_groups is None else n_groups
+        self.sample = list(sample)
+        self.host_all = (self.G <= 64) if host_all is None else host_all
+        if self.host_all:
+            self.sample = list(range(self.G))
+        self.st = NystromStates(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.d,
+                                wl.dv, self.G, wl.rect, device)
+        self.flagged = 0
+        self.checked = 0
+        self.worst = 0.0
+        self.fill = None if self.host_all else DeviceFill(
+            wl.with_(seqs=1, layers=1, kv_groups=self.G), device)
+
+    # ------------------------------------------------------------ seal
+    def seal(self):
+        torch, wl, G = self.torch, self.wl, self.G
+        qh, kh, vh, self.gens = host_prompt_batch(wl, self.sample)
+        if self.host_all:
+            q = torch.from_numpy(qh).to(self.dev)
+            k = torch.from_numpy(kh).to(self.dev)
+            v = torch.from_numpy(vh).to(self.dev)
+        else:
+            q = torch.empty((G, wl.heads_per_kv, wl.t, wl.d), device=self.dev)
+            k = torch.empty((G, wl.t, wl.d), device=self.dev)
+            v = torch.empty((G, wl.t, wl.dv), device=self.dev)
+            self.fill.prompt_into(q, k, v)
+            idx = torch.tensor(self.sample, device=self.dev)
+            q[idx] = torch.from_numpy(qh).to(self.dev)
+            k[idx] = torch.from_numpy(kh).to(self.dev)
+            v[idx] = torch.from_numpy(vh).to(self.dev)
+        self.st.seal(q, k, v)
+        torch.cuda.synchronize(self.dev)
+        del q, k, v
+        self.oracles = []
+        for i, g in enumerate(self.sample):
+            o = NystromOracle(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.rect)
+            o.prefill(qh[i], kh[i], vh[i])
+            self.oracles.append(o)
+        self.n_steps = 0
+
+    # ------------------------------------------------------------ state
+    def check_state(self, far_tol=FAR_TOL):
+        """Compare every sampled group's device state with its oracle."""
+        torch = self.torch
+        st = self.st
+        reg = {name: st.region(name).cpu().numpy() for name in (
+            "win_k", "win_v", "sink_k", "sink_v", "k_tilde", "q_tilde", "mu",
+            "t_hat", "z_hat", "m_max", "far_len", "ints")}
+        for o, g in zip(self.oracles, self.sample):
+            me = o.m_eff
+            ints = reg["ints"][g]
+            assert ints[0] == o.win_head and ints[1] == o.win_len, (g, ints)
+            assert ints[2] == me and ints[4] == 1, (g, ints)
+            np.testing.assert_array_equal(reg["win_k"][g], o.win_k.astype(np.float32))
+            np.testing.assert_array_equal(reg["win_v"][g], o.win_v.astype(np.float32))
+            if o.sink_len:
+                np.testing.assert_array_equal(reg["sink_k"][g], o.sink_k.astype(np.float32))
+                np.testing.assert_array_equal(reg["sink_v"][g], o.sink_v.astype(np.float32))
+            kt = reg["k_tilde"][g][:me].astype(np.float64)
+            _close_rows(kt, o.k_tilde, LANDMARK_TOL, "k_tilde", g)
+            for h, hs in enumerate(o.hs):
+                assert reg["far_len"][g][h] == hs.far_len, (g, h)
+                _close_rows(reg["q_tilde"][g][h][:me].astype(np.float64),
+                            hs.q_tilde, LANDMARK_TOL, "q_tilde", g)
+                mu = reg["mu"][g][h][:me, :me].astype(np.float64)
+                rel = np.linalg.norm(mu - hs.mu) / np.linalg.norm(hs.mu)
+                assert rel <= MU_TOL, ("mu", g, h, rel)
+                mm = reg["m_max"][g][h][:me].astype(np.float64)
+                assert np.all(np.abs(mm - hs.m_max) <= far_tol * np.maximum(1.0, np.abs(hs.m_max))), \
+                    ("m_max", g, h, np.abs(mm - hs.m_max).max())
+                # Bring the device accumulators to the oracle's scale.
+                rescale = np.exp(mm - hs.m_max)
+                z = reg["z_hat"][g][h][:me].astype(np.float64) * rescale
+                np.testing.assert_allclose(z, hs.z_hat, rtol=far_tol, atol=0)
+                t = reg["t_hat"][g][h][:me].astype(np.float64) * rescale[:, None]
+                for b in range(me):
+                    e = row_err(t[b], hs.t_hat[b])
+                    assert e <= far_tol, ("t_hat", g, h, b, e)
+
+    # ------------------------------------------------------------ decode
+    def step(self):
+        torch, wl, G = self.torch, self.wl, self.G
+        n = self.n_steps
+        qh, kh, vh = host_token_batch(self.gens, n)
+        if self.host_all:
+            q = torch.from_numpy(qh).to(self.dev)
+            k = torch.from_numpy(kh).to(self.dev)
+            v = torch.from_numpy(vh).to(self.dev)
+        else:
+            q = torch.empty((1, G, wl.heads_per_kv, wl.d), device=self.dev)
+            k = torch.empty((1, G, wl.d), device=self.dev)
+            v = torch.empty((1, G, wl.dv), device=self.dev)
+            self.fill.tokens_into(q, k, v)
+            q, k, v = q[0], k[0], v[0]
+            idx = torch.tensor(self.sample, device=self.dev)
+            q[idx] = torch.from_numpy(qh).to(self.dev)
+            k[idx] = torch.from_numpy(kh).to(self.dev)
+            v[idx] = torch.from_numpy(vh).to(self.dev)
+        out = torch.empty((G, wl.heads_per_kv, wl.dv), device=self.dev)
+        self.st.step(q, k, v, out)
+        got = out[torch.tensor(self.sample, device=self.dev)].cpu().numpy()
+        self.n_steps += 1
+        for i, o in enumerate(self.oracles):
+            ref = o.step(qh[i], kh[i], vh[i])
+            for h in range(wl.heads_per_kv):
+                dg = o.diags[-1][h]
+                err = row_err(got[i, h].astype(np.float64), ref[h])
+                self.checked += 1
+                if abs(dg.margin) < GUARD_BAND or dg.near_gap > UNDERFLOW_GAP:
+                    self.flagged += 1
+                    assert np.all(np.isfinite(got[i, h]))
+                    continue
+                self.worst = max(self.worst, err)
+                assert err <= OUT_TOL, (self.sample[i], h, n, err)
+        return out
+
+    def check_counters_all(self):
+        """Properties that hold for every group at any size: counters follow
+        the eviction count exactly."""
+        wl = self.wl
+        far = self.st.region("far_len").cpu().numpy()
+        ints = self.st.region("ints").cpu().numpy()
+        ev = wl.t - wl.sink - wl.w + self.n_steps
+        assert np.all(far == ev), (far.min(), far.max(), ev)
+        assert np.all(ints[:, 0] == (wl.t - wl.sink + self.n_steps) % wl.w)
+        assert np.all(ints[:, 1] == wl.w)
+
+    def close(self):
+        self.st.close()
+
+
+def _close_rows(got, ref, tol, what, g):
+    scale = np.maximum(np.abs(ref).max(axis=1, keepdims=True), 1e-30)
+    err = float((np.abs(got - ref) / scale).max())
+    assert err <= tol, (what, g, err)
