@@ -40,13 +40,15 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "step_kernel_batch64.txt")
 
 
 def algorithmic_bytes(wl) -> int:
-    """Bytes one group-step must move at minimum (fp32): the window read, the
-    sinks, K~, the new k/v read and written into the ring; per head Q~, M,
-    T^ read and written, Z^ and m_max read and written, q and the output."""
+    """Bytes one group-step must move at minimum: the window read, the sinks,
+    K~, the new k/v read and written into the ring (fp32); per head Q~, M,
+    T^ read and written, Z^ and m_max read and written, q and the output
+    (fp32), plus the low parts of T^ (bf16) and Z^ (fp32) read and written."""
     f, H, m, w, s, d, dv = 4, wl.heads_per_kv, wl.m, wl.w, wl.sink, wl.d, wl.dv
     shared = f * (w * (d + dv) + s * (d + dv) + m * d + 2 * (d + dv))
     head = f * (m * d + m * m + 2 * m * dv + 4 * m + d + dv)
-    return shared + H * head
+    low = 2 * 2 * m * dv + 2 * 4 * m
+    return shared + H * (head + low)
 
 
 def workload_config(wl, extra=None):
@@ -385,11 +387,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-groups", type=int, default=3)
+    ap.add_argument("--groups", type=int, default=0,
+                    help="override the workload's group count (profiling on a "
+                         "smaller case); 0 keeps the workload's own")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from streaming_nystr_landmark_gb300.workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.groups:
+        wl = wl.with_(name=f"{wl.name}[{args.groups} groups]", seqs=1, layers=1,
+                      kv_groups=args.groups)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

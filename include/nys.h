@@ -93,17 +93,28 @@ typedef struct nys_states nys_states; /* opaque host handle */
  *   q_tilde f32 [G][H][m][d]     query landmarks Q~ (per head)
  *   mu      f32 [G][H][m][m]     M: row = key landmark a, column = query
  *                                landmark b
- *   t_hat   f32 [G][H][m][dv]    far numerator at scale e^{-m_max}
- *   z_hat   f32 [G][H][m]        far denominator, same scale
+ *   t_hat   f32 [G][H][m][dv]    far numerator at scale e^{-m_max} (high part)
+ *   z_hat   f32 [G][H][m]        far denominator, same scale (high part)
  *   m_max   f32 [G][H][m]        per-landmark running max of far logits
+ *   t_lo    bf16 [G][H][m][dv]   low part of the far numerator
+ *   z_lo    f32 [G][H][m]        low part of the far denominator
  *   far_len i32 [G][H]           keys absorbed per head
  *   ints    i32 [G][8]           {win_head, win_len, m_eff, t, mode, 0, 0, 0},
  *                                mode 0 = empty, 1 = sealed (landmark path)
+ *
+ * The far accumulators are carried as unevaluated sums T^ = t_hat + t_lo and
+ * Z^ = z_hat + z_lo.  The page keeps them as plain f32; every decode token
+ * rounds them once more, and the ill-conditioned mixing F^ M amplifies that
+ * drift roughly fifty-fold in the output, so over a thousand tokens plain f32
+ * leaves the exact result by ~1e-4.  The low parts hold the rounding error of
+ * each update (exact product and sum errors via FMA), which keeps the far
+ * field within ~1e-7 of exact at 12.5% more state bytes.
  */
 typedef struct {
   size_t total_bytes;
   size_t off_win_k, off_win_v, off_sink_k, off_sink_v, off_k_tilde;
   size_t off_q_tilde, off_mu, off_t_hat, off_z_hat, off_m_max;
+  size_t off_t_lo, off_z_lo;
   size_t off_far_len, off_ints;
   int64_t n_groups;
   int32_t ints_per_group; /* 8 */

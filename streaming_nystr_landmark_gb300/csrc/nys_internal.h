@@ -44,11 +44,47 @@ struct DevState {
   float* t_hat;
   float* z_hat;
   float* m_max;
+  uint16_t* t_lo;  // bf16 bits: low part of t_hat
+  float* z_lo;     // low part of z_hat
   int32_t* far_len;
   int32_t* ints;
   int32_t m, w, sink, heads, d, dv, rect;
   float scale;  // 1/sqrt(d) evaluated in f32
 };
+
+#ifdef __CUDACC__
+// Compensated update of an unevaluated sum hi + lo:
+//   (hi + lo) * r + x * y  ->  (nhi, nlo),  nhi = fl(value), nlo = remainder.
+// The product errors come exactly from FMA (a*b - fl(a*b)), the sum error from
+// Knuth's two-sum, so the pair tracks the update to ~2^-48 relative instead of
+// rounding it to 2^-24 each time.  Used for the far accumulators T^ and Z^.
+__device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, float y,
+                                          float& nhi, float& nlo) {
+  const float a = hi * r;
+  const float pa = fmaf(hi, r, -a);
+  const float b = x * y;
+  const float pb = fmaf(x, y, -b);
+  const float s = a + b;
+  const float sb = s - a;
+  const float es = (a - (s - sb)) + (b - sb);
+  const float t = fmaf(lo, r, pa + pb + es);
+  nhi = s + t;
+  const float tb = nhi - s;
+  nlo = (s - (nhi - tb)) + (t - tb);
+}
+
+// bf16 storage of a low part: bits of the upper half of an f32, rounded to
+// nearest even; the round trip is exact for values that fit.
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+__device__ __forceinline__ uint32_t f32_to_bf16(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (u >> 16) | ((u & 0xffffu) ? 0x40u : 0u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+#endif
 
 // One decode token for groups [g0, g0+n): one kernel launch on `stream`.
 cudaError_t launch_step(const DevState& s, int64_t g0, int64_t n,

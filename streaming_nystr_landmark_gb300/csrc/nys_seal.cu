@@ -22,7 +22,9 @@
 //     exp(l_ij - m_max_i), T^_i = sum_j exp(l_ij - m_max_i) v_j with
 //     l_ij = (q~_i . k_j) * scale in f32; this kernel reaches it with a
 //     blocked online maximum (flash-style rescale per block of keys), which
-//     changes only the rounding order.
+//     changes only the rounding order, and folds each block's sums into
+//     compensated (hi, lo) accumulators so that tens of thousands of
+//     evictions do not accumulate f32 rounding.
 #include <cfloat>
 #include <cmath>
 
@@ -275,44 +277,59 @@ pinv_kernel(DevState s, int64_t g0, int m_eff, const double* __restrict__ ws) {
 
 // ---------------------------------------------------------------- 3
 constexpr int kKeyBlock = 32;
+constexpr int kValTile = 128;  // value columns per block (grid.y tiles dv)
 
 struct ReplaySmem {
-  int qt, kb, vb, p, acc, rmax, zacc, alpha, total, dp, pp;
-  __host__ __device__ ReplaySmem(int me, int d, int dv) {
-    dp = d + 4;          // skewed rows: float4 reads across lanes hit all banks
+  int qt, kb, vb, p, hi, lo, rmax, zhi, zlo, alpha, total, dp, pp;
+  __host__ __device__ ReplaySmem(int me, int d) {
+    dp = d + 4;  // skewed rows: float4 reads across lanes hit all banks
     pp = kKeyBlock + 1;
+    const int m4 = (me + 3) & ~3;
     int o = 0;
     qt = o;    o += me * dp;
     kb = o;    o += kKeyBlock * dp;
-    vb = o;    o += kKeyBlock * dv;
+    vb = o;    o += kKeyBlock * kValTile;
     p = o;     o += ((me * pp + 3) & ~3);
-    acc = o;   o += me * dv;
-    rmax = o;  o += (me + 3) & ~3;
-    zacc = o;  o += (me + 3) & ~3;
-    alpha = o; o += (me + 3) & ~3;
+    hi = o;    o += me * kValTile;
+    lo = o;    o += me * kValTile;
+    rmax = o;  o += m4;
+    zhi = o;   o += m4;
+    zlo = o;   o += m4;
+    alpha = o; o += m4;
     total = o;
   }
 };
 
+// One block per (group, head, value tile).  Keys are consumed in blocks of
+// kKeyBlock: logits L = Q~ K_blk^T * scale, a per-landmark online maximum,
+// block sums of exp(L - max) and of exp(L - max) v, and a compensated fold of
+// each block sum into the running (hi, lo) accumulators.  Every value tile
+// recomputes the same logits, so the tile with blockIdx.y == 0 alone writes
+// m_max and Z^.
 __global__ void __launch_bounds__(kThreads)
 replay_kernel(DevState s, int64_t g0, int t, int m_eff,
               const float* __restrict__ k, const float* __restrict__ v) {
   extern __shared__ __align__(16) float fsm[];
   const int tid = threadIdx.x;
   const int H = s.heads, m = s.m, d = s.d, dv = s.dv, w = s.w, ns = s.sink;
-  const int d4 = d >> 2, dv4 = dv >> 2, me = m_eff;
+  const int d4 = d >> 2, me = m_eff;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
   const int h = (int)(blockIdx.x - gi * H);
   const int64_t hb = g * H + h;
+  const int c0 = blockIdx.y * kValTile;
+  const int cw = min(kValTile, dv - c0);
+  const int cw4 = cw >> 2;
   const float scale = s.scale;
-  const ReplaySmem L(me, d, dv);
+  const ReplaySmem L(me, d);
   float* qt = fsm + L.qt;
   float* kb = fsm + L.kb;
   float* vb = fsm + L.vb;
   float* P = fsm + L.p;
-  float* acc = fsm + L.acc;
+  float* ahi = fsm + L.hi;
+  float* alo = fsm + L.lo;
   float* rmax = fsm + L.rmax;
-  float* zacc = fsm + L.zacc;
+  float* zhi = fsm + L.zhi;
+  float* zlo = fsm + L.zlo;
   float* alpha = fsm + L.alpha;
 
   const float* qsrc = s.q_tilde + hb * m * (int64_t)d;
@@ -322,12 +339,16 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
   }
   for (int i = tid; i < me; i += kThreads) {
     rmax[i] = -INFINITY;
-    zacc[i] = 0.f;
+    zhi[i] = 0.f;
+    zlo[i] = 0.f;
   }
-  for (int idx = tid; idx < me * dv; idx += kThreads) acc[idx] = 0.f;
+  for (int idx = tid; idx < me * kValTile; idx += kThreads) {
+    ahi[idx] = 0.f;
+    alo[idx] = 0.f;
+  }
 
   const float* ksrc = k + gi * (int64_t)t * d;
-  const float* vsrc = v + gi * (int64_t)t * dv;
+  const float* vsrc = v + gi * (int64_t)t * dv + c0;
   const int j_end = t - w;  // keys sink .. t-w-1 were evicted by the replay
   for (int j0 = ns; j0 < j_end; j0 += kKeyBlock) {
     const int nb = min(kKeyBlock, j_end - j0);
@@ -335,9 +356,9 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
       const int jj = idx / d4, c = idx - jj * d4;
       st4(kb + jj * L.dp + 4 * c, ld4(ksrc + (int64_t)(j0 + jj) * d + 4 * c));
     }
-    for (int idx = tid; idx < nb * dv4; idx += kThreads) {
-      const int jj = idx / dv4, c = idx - jj * dv4;
-      st4(vb + jj * dv + 4 * c, ld4(vsrc + (int64_t)(j0 + jj) * dv + 4 * c));
+    for (int idx = tid; idx < nb * cw4; idx += kThreads) {
+      const int jj = idx / cw4, c = idx - jj * cw4;
+      st4(vb + jj * kValTile + 4 * c, ld4(vsrc + (int64_t)(j0 + jj) * dv + 4 * c));
     }
     __syncthreads();
     for (int p = tid; p < me * nb; p += kThreads) {
@@ -358,34 +379,45 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
       const float old = rmax[i];
       const float nm = fmaxf(old, bm);
       const float a = (old == -INFINITY) ? 0.f : expf(old - nm);
-      float z = zacc[i] * a;
+      float zb = 0.f;
       for (int jj = 0; jj < nb; ++jj) {
         const float e = expf(P[i * L.pp + jj] - nm);
         P[i * L.pp + jj] = e;
-        z += e;
+        zb += e;
       }
-      zacc[i] = z;
+      float nh, nl;
+      comp_axpy(zhi[i], zlo[i], a, zb, 1.f, nh, nl);
+      zhi[i] = nh;
+      zlo[i] = nl;
       rmax[i] = nm;
       alpha[i] = a;
     }
     __syncthreads();
-    for (int p = tid; p < me * dv; p += kThreads) {
-      const int i = p / dv, c = p - i * dv;
-      float x = acc[p] * alpha[i];
-      for (int jj = 0; jj < nb; ++jj) x = fmaf(P[i * L.pp + jj], vb[jj * dv + c], x);
-      acc[p] = x;
+    for (int p = tid; p < me * cw; p += kThreads) {
+      const int i = p / cw, c = p - i * cw;
+      float part = 0.f;
+      for (int jj = 0; jj < nb; ++jj) part = fmaf(P[i * L.pp + jj], vb[jj * kValTile + c], part);
+      float nh, nl;
+      comp_axpy(ahi[i * kValTile + c], alo[i * kValTile + c], alpha[i], part, 1.f, nh, nl);
+      ahi[i * kValTile + c] = nh;
+      alo[i * kValTile + c] = nl;
     }
     __syncthreads();
   }
 
-  for (int i = tid; i < me; i += kThreads) {
-    s.m_max[hb * m + i] = rmax[i];
-    s.z_hat[hb * m + i] = zacc[i];
+  if (blockIdx.y == 0) {
+    for (int i = tid; i < me; i += kThreads) {
+      s.m_max[hb * m + i] = rmax[i];
+      s.z_hat[hb * m + i] = zhi[i];
+      s.z_lo[hb * m + i] = zlo[i];
+    }
   }
-  float* tdst = s.t_hat + hb * m * (int64_t)dv;
-  for (int idx = tid; idx < me * dv; idx += kThreads) {
-    const int i = idx / dv, c = idx - i * dv;
-    tdst[(int64_t)i * dv + c] = acc[idx];
+  float* tdst = s.t_hat + hb * m * (int64_t)dv + c0;
+  uint16_t* ldst = s.t_lo + hb * m * (int64_t)dv + c0;
+  for (int p = tid; p < me * cw; p += kThreads) {
+    const int i = p / cw, c = p - i * cw;
+    tdst[(int64_t)i * dv + c] = ahi[i * kValTile + c];
+    ldst[(int64_t)i * dv + c] = (uint16_t)f32_to_bf16(alo[i * kValTile + c]);
   }
 }
 
@@ -415,10 +447,11 @@ cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
   pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, m_eff, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const ReplaySmem R(m_eff, s.d, s.dv);
+  const ReplaySmem R(m_eff, s.d);
   const size_t rbytes = (size_t)R.total * sizeof(float);
   if ((e = set_smem((const void*)replay_kernel, rbytes)) != cudaSuccess) return e;
-  replay_kernel<<<(unsigned)(n * s.heads), kThreads, rbytes, stream>>>(
+  const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
+  replay_kernel<<<dim3((unsigned)(n * s.heads), tiles), kThreads, rbytes, stream>>>(
       s, g0, t, m_eff, k, v);
   return cudaGetLastError();
 }

@@ -11,7 +11,7 @@
 //                                landmark row with its own shift f, u = F^ M
 //                                (Fm clamp), joint shift c_all, Aggregate
 //                                guard, one division floored at 1e-30.
-// All state stays fp32, as on the page.
+// State is fp32 as on the page; the far accumulators also carry a low part.
 //
 // Work split inside the CTA (8 warps):
 //   A  every shared K-side row (sinks, window, key landmarks) is read once and
@@ -24,6 +24,10 @@
 //      heads; each head's T^ row is read, updated with the evicted value,
 //      written back and accumulated in the same pass, so T^ crosses HBM once
 //      each way.  Partial sums are reduced across warps in shared memory.
+// T^ and Z^ are carried as hi + lo pairs (fp32 + bf16 / fp32) updated with
+// exact FMA product errors and two-sum, so the decode's thousands of
+// accumulations do not drift (plain f32 drifts ~1e-6 in T^ per thousand
+// tokens, which the ill-conditioned mixing row amplifies into the output).
 // The new key/value are written into the ring slot after every read of the
 // old slot content (the page's ordering: absorb first, then overwrite).
 #include <cfloat>
@@ -212,9 +216,10 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
       float* hms = ms + hh * L.mp;
       float* hsig = sig + hh * L.nrp;
       const int32_t fl = s.far_len[hb];
+      float* zl = s.z_lo + hb * m;
       for (int i = lane; i < m_eff; i += 32) {
-        const float mo = mx[i], zo = zh[i];
-        float r = 1.f, e = 0.f, mn = mo, zn = zo;
+        const float mo = mx[i], zo = zh[i], zlo = zl[i];
+        float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
         if (full) {
           const float l = lg[hh * L.mp + i];
           if (l > mo) {
@@ -222,13 +227,14 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
             mn = l;
           }
           e = expf(l - mn);
-          zn = zo * r + e;
+          comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
           mx[i] = mn;
           zh[i] = zn;
+          zl[i] = zln;
         }
         rs[hh * L.mp + i] = r;
         es[hh * L.mp + i] = e;
-        hzs[i] = zn;
+        hzs[i] = zn + zln;
         hms[i] = mn;
       }
       const int32_t fl_new = fl + (full ? 1 : 0);
@@ -313,22 +319,30 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
           const int64_t hb = g * H + h0 + hh;
           for (int b = warp; b < m_eff; b += kWarps) {
             float* trow = s.t_hat + (hb * m + b) * (int64_t)dv;
+            uint2* lrow = reinterpret_cast<uint2*>(s.t_lo + (hb * m + b) * (int64_t)dv);
             if (cv) {
               float4 x = ld4(trow + 4 * c4);
+              const uint2 lr = lrow[c4];
+              float4 lo = make_float4(bf16_to_f32(lr.x & 0xffffu), bf16_to_f32(lr.x >> 16),
+                                      bf16_to_f32(lr.y & 0xffffu), bf16_to_f32(lr.y >> 16));
               if (full) {
                 const float r = rs[hh * L.mp + b], e = es[hh * L.mp + b];
                 const float4 ve = ld4(vev + 4 * c4);
-                x.x = fmaf(e, ve.x, x.x * r);
-                x.y = fmaf(e, ve.y, x.y * r);
-                x.z = fmaf(e, ve.z, x.z * r);
-                x.w = fmaf(e, ve.w, x.w * r);
+                comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
+                comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
+                comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
+                comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
                 st4(trow + 4 * c4, x);
+                uint2 lw;
+                lw.x = f32_to_bf16(lo.x) | (f32_to_bf16(lo.y) << 16);
+                lw.y = f32_to_bf16(lo.z) | (f32_to_bf16(lo.w) << 16);
+                lrow[c4] = lw;
               }
               const float gb = gs[hh * L.mp + b];
-              acc[hh].x = fmaf(gb, x.x, acc[hh].x);
-              acc[hh].y = fmaf(gb, x.y, acc[hh].y);
-              acc[hh].z = fmaf(gb, x.z, acc[hh].z);
-              acc[hh].w = fmaf(gb, x.w, acc[hh].w);
+              acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
+              acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
+              acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
+              acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
             }
           }
         }

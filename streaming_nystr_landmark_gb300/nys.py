@@ -47,6 +47,7 @@ class NysLayout(ctypes.Structure):
                 ("off_k_tilde", ctypes.c_size_t), ("off_q_tilde", ctypes.c_size_t),
                 ("off_mu", ctypes.c_size_t), ("off_t_hat", ctypes.c_size_t),
                 ("off_z_hat", ctypes.c_size_t), ("off_m_max", ctypes.c_size_t),
+                ("off_t_lo", ctypes.c_size_t), ("off_z_lo", ctypes.c_size_t),
                 ("off_far_len", ctypes.c_size_t), ("off_ints", ctypes.c_size_t),
                 ("n_groups", ctypes.c_int64), ("ints_per_group", ctypes.c_int32)]
 
@@ -256,6 +257,8 @@ class NystromStates:
             "t_hat": (torch.float32, (G, H, m, c.dv)),
             "z_hat": (torch.float32, (G, H, m)),
             "m_max": (torch.float32, (G, H, m)),
+            "t_lo": (torch.bfloat16, (G, H, m, c.dv)),
+            "z_lo": (torch.float32, (G, H, m)),
             "far_len": (torch.int32, (G, H)),
             "ints": (torch.int32, (G, self.layout.ints_per_group)),
         }
@@ -264,8 +267,17 @@ class NystromStates:
         count = 1
         for s in shape:
             count *= s
-        raw = self.buf[off: off + 4 * count]
+        size = 2 if dtype == torch.bfloat16 else 4
+        raw = self.buf[off: off + size * count]
         return raw.view(dtype).view(shape)
+
+    def far_numerator(self):
+        """T^ = t_hat + t_lo as float64 on the host (test helper)."""
+        return (self.region("t_hat").double() + self.region("t_lo").double()).cpu().numpy()
+
+    def far_denominator(self):
+        """Z^ = z_hat + z_lo as float64 on the host (test helper)."""
+        return (self.region("z_hat").double() + self.region("z_lo").double()).cpu().numpy()
 
     def mark_sealed(self, g0=0, n=None):
         nys_mark_sealed(self.handle, g0, self.n_groups if n is None else n)

@@ -14,7 +14,8 @@ Tolerances (derived from fp32 evaluation of the step):
                   underflow by design of the joint shift);
   K~, Q~          <= 1e-6 relative to the row's max magnitude;
   M               <= 1e-5 normwise relative;
-  T^, Z^, m_max   <= 1e-5, compared at a common scale;
+  T^, Z^, m_max   <= 1e-5, compared at a common scale (T^ and Z^ are the
+                  device's hi + lo pairs);
   window, sinks   bit-exact (copies of the inputs);
   counters        bit-exact (far_len per head, win_head, win_len, m_eff, t).
 """
@@ -93,7 +94,9 @@ class ParityRun:
         st = self.st
         reg = {name: st.region(name).cpu().numpy() for name in (
             "win_k", "win_v", "sink_k", "sink_v", "k_tilde", "q_tilde", "mu",
-            "t_hat", "z_hat", "m_max", "far_len", "ints")}
+            "m_max", "far_len", "ints")}
+        reg["t_hat"] = st.far_numerator()
+        reg["z_hat"] = st.far_denominator()
         for o, g in zip(self.oracles, self.sample):
             me = o.m_eff
             ints = reg["ints"][g]
