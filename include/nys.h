@@ -52,8 +52,10 @@ typedef enum {
   NYS_E_BUF = -5,        /* caller buffer smaller than nys_memory_bytes       */
   NYS_E_ALIGN = -6,      /* pointer not 16-byte aligned (state: 256-byte)     */
   NYS_E_CUDA = -7,       /* a CUDA call or kernel launch failed               */
-  NYS_E_UNSUPPORTED = -8 /* geometry beyond the kernels' limits: m > 64,
+  NYS_E_UNSUPPORTED = -8, /* geometry beyond the kernels' limits: m > 64,
                             d or dv > 256, heads_per_kv > 64, sink + w > 2048  */
+  NYS_E_SCRATCH = -9     /* nys_seal_static only: one group's workspace does
+                            not fit the library's static scratch array         */
 } nys_status;
 
 /* Rectifier of the skeleton's far mass (nystrom.rs, enum O1Rect).
@@ -187,6 +189,32 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t,
  * NYS_E_CUDA. */
 int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
                    const float* k, const float* v, float* out, void* stream);
+
+/* nys_seal without any device allocation.  The pages have no counterpart:
+ * this entry point exists for callers that must not allocate device memory
+ * while they run -- a serving loop that has reserved all memory up front, an
+ * allocator that forbids cudaMalloc/cudaMallocAsync inside its critical
+ * section, or code embedded in a host application that owns every buffer.
+ * It computes exactly what nys_seal computes (same kernels, same checks,
+ * same results), but its f64 landmark workspace is a 4 MiB array that the
+ * library places in device global memory at load time (every GPU that loads
+ * the library keeps those 4 MiB until the process exits).  Groups are sealed
+ * in chunks that fit the array, one after another on `stream`.
+ *  - The first call on a device looks the array's device address up
+ *    (cudaGetSymbolAddress) with that device current and caches it; make
+ *    that first call before any stream capture on the device.
+ *  - Every call on a device shares the one array, and each call overwrites
+ *    what the previous one left there.  Calls that may run at the same time
+ *    on the GPU (different streams without ordering between them) race on
+ *    it: order them on one stream or with events.
+ *  - A geometry whose single-group workspace, (1 + heads_per_kv) * m * d * 8
+ *    bytes, exceeds 4 MiB is rejected with NYS_E_SCRATCH before anything is
+ *    enqueued.
+ * Arguments, layouts and the other errors are those of nys_seal (NYS_E_INVAL,
+ * NYS_E_RANGE, NYS_E_EXACT_ONLY, NYS_E_ALIGN, NYS_E_CUDA). */
+int nys_seal_static(nys_states* st, int64_t g0, int64_t n, int32_t t,
+                    const float* q, const float* k, const float* v,
+                    void* stream);
 
 /* Read one group's counters to the host (nystrom.rs, NystromState::far_len,
  * and the O1DeviceView scalars).  far_len, if not NULL, receives

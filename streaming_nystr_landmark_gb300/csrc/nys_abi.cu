@@ -118,6 +118,37 @@ std::atomic<bool> g_clamp_said{false};
 
 }  // namespace
 
+namespace nys {
+
+int prepare_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
+                 const float* k, const float* v, DevState* ds, int* m_eff) {
+  if (!st || !ds || !m_eff) return NYS_E_INVAL;
+  int rc = check_range(st, g0, n);
+  if (rc) return rc;
+  const nys_config& c = st->cfg;
+  if (t < 1) return NYS_E_RANGE;
+  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) return NYS_E_EXACT_ONLY;
+  if (n > 0) {
+    if (!q || !k || !v) return NYS_E_INVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
+  }
+  *m_eff = std::min(std::max(t / 8, 4), c.m);
+  if (n > 0 && *m_eff < c.m && !g_clamp_said.exchange(true)) {
+    std::fprintf(stderr,
+                 "nys: landmark budget m=%d clamped to m_eff=%d: the prompt is %d tokens and "
+                 "the landmarks take t/8; seal at least %d tokens to use the whole budget\n",
+                 c.m, *m_eff, t, c.m * 8);
+  }
+  *ds = dev_state(st);
+  return NYS_OK;
+}
+
+void record_sealed(nys_states* st, int64_t g0, int64_t n) {
+  if (n > 0) std::memset(st->sealed.data() + g0, 1, (size_t)n);
+}
+
+}  // namespace nys
+
 extern "C" {
 
 const char* nys_strerror(int status) {
@@ -133,6 +164,9 @@ const char* nys_strerror(int status) {
     case NYS_E_CUDA: return "CUDA error";
     case NYS_E_UNSUPPORTED:
       return "geometry beyond kernel limits (m <= 64, d, dv <= 256, heads <= 64, sink + w <= 2048)";
+    case NYS_E_SCRATCH:
+      return "one group's seal workspace, (1 + heads_per_kv) * m * d * 8 bytes, exceeds the "
+             "4 MiB static scratch of nys_seal_static; use nys_seal";
     default: return "unknown status";
   }
 }

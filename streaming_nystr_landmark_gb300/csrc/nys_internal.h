@@ -102,4 +102,13 @@ cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
                         const float* v, double* ws, cudaStream_t stream);
 
+// Host-side checks of a seal request, identical to nys_seal's, for entry
+// points that supply their own workspace.  Fills the device view and m_eff
+// (printing the one-time clamp notice); returns a nys_status.
+int prepare_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
+                 const float* k, const float* v, DevState* ds, int* m_eff);
+
+// Host record that groups [g0, g0+n) hold a sealed state.
+void record_sealed(nys_states* st, int64_t g0, int64_t n);
+
 }  // namespace nys

@@ -24,13 +24,15 @@ NYS_E_BUF = -5
 NYS_E_ALIGN = -6
 NYS_E_CUDA = -7
 NYS_E_UNSUPPORTED = -8
+NYS_E_SCRATCH = -9
 NYS_RECT_AGGREGATE = 0
 NYS_RECT_FM = 1
 
 # Every entry point include/nys.h declares.
 EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
             "nys_seal", "nys_step_batch", "nys_query", "nys_layout_of",
-            "nys_mark_sealed", "nys_config_of", "nys_strerror")
+            "nys_mark_sealed", "nys_config_of", "nys_strerror",
+            "nys_seal_static")
 
 
 class NysConfig(ctypes.Structure):
@@ -76,6 +78,7 @@ def _load():
         "nys_mark_sealed": [VP, I64, I64],
         "nys_config_of": [VP, P(NysConfig), P(I64)],
         "nys_strerror": [ctypes.c_int],
+        "nys_seal_static": [VP, I64, I64, I32, VP, VP, VP, VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -127,6 +130,13 @@ def nys_free_states(handle: int):
 
 def nys_seal(handle, g0, n, t, q, k, v, stream=0):
     _check(_lib.nys_seal(handle, g0, n, t, q, k, v, stream or None), "nys_seal")
+
+
+def nys_seal_static(handle, g0, n, t, q, k, v, stream=0):
+    """nys_seal with the library's static workspace instead of an allocation
+    (for callers that cannot allocate device memory while they run)."""
+    _check(_lib.nys_seal_static(handle, g0, n, t, q, k, v, stream or None),
+           "nys_seal_static")
 
 
 def nys_step_batch(handle, g0, n, q, k, v, out, stream=0):
