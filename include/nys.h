@@ -101,8 +101,11 @@ typedef struct nys_states nys_states; /* opaque host handle */
  *   t_lo    bf16 [G][H][m][dv]   low part of the far numerator
  *   z_lo    f32 [G][H][m]        low part of the far denominator
  *   far_len i32 [G][H]           keys absorbed per head
- *   ints    i32 [G][8]           {win_head, win_len, m_eff, t, mode, 0, 0, 0},
- *                                mode 0 = empty, 1 = sealed (landmark path)
+ *   ints    i32 [G][8]           {win_head, win_len, m_eff, t, mode, status, 0, 0},
+ *                                mode 0 = empty, 1 = sealed (landmark path);
+ *                                status 0 = fine, nonzero = a bounded wait in a
+ *                                decode kernel gave up (every wait is limited
+ *                                to 2 s); that group's state is then invalid
  *
  * The far accumulators are carried as unevaluated sums T^ = t_hat + t_lo and
  * Z^ = z_hat + z_lo.  The page keeps them as plain f32; every decode token

@@ -27,6 +27,7 @@ enum : int {
   kIntMEff = 2,
   kIntT = 3,
   kIntMode = 4,
+  kIntStatus = 5,  // nonzero: a bounded wait in the step kernel gave up
   kIntsPerGroup = 8
 };
 enum : int { kModeEmpty = 0, kModeSealed = 1 };
@@ -58,38 +59,50 @@ struct DevState {
 // The product errors come exactly from FMA (a*b - fl(a*b)), the sum error from
 // Knuth's two-sum, so the pair tracks the update to ~2^-48 relative instead of
 // rounding it to 2^-24 each time.  Used for the far accumulators T^ and Z^.
+// r == 1 (no new running maximum, the common case) skips the rescale terms.
 __device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, float y,
                                           float& nhi, float& nlo) {
-  const float a = hi * r;
-  const float pa = fmaf(hi, r, -a);
   const float b = x * y;
   const float pb = fmaf(x, y, -b);
+  float a = hi, t0 = pb;
+  if (r != 1.f) {
+    a = hi * r;
+    t0 += fmaf(hi, r, -a);
+    lo *= r;
+  }
   const float s = a + b;
   const float sb = s - a;
   const float es = (a - (s - sb)) + (b - sb);
-  const float t = fmaf(lo, r, pa + pb + es);
+  const float t = lo + (t0 + es);
   nhi = s + t;
-  const float tb = nhi - s;
-  nlo = (s - (nhi - tb)) + (t - tb);
+  nlo = t - (nhi - s);
 }
 
-// bf16 storage of a low part: bits of the upper half of an f32, rounded to
-// nearest even; the round trip is exact for values that fit.
-__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
-  return __uint_as_float(bits16 << 16);
+// bf16 storage of low parts: two values per 32-bit word, round to nearest
+// even (hardware conversion).
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
 }
-__device__ __forceinline__ uint32_t f32_to_bf16(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u & 0x7f800000u) == 0x7f800000u) return (u >> 16) | ((u & 0xffffu) ? 0x40u : 0u);
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return u >> 16;
-}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 #endif
 
 // One decode token for groups [g0, g0+n): one kernel launch on `stream`.
 cudaError_t launch_step(const DevState& s, int64_t g0, int64_t n,
                         const float* q, const float* k, const float* v,
                         float* out, cudaStream_t stream);
+
+// Fast path of the step (nys_step_tma.cu): plan_step_tma fills an opaque
+// plan of at most kPlanBytes and returns false for geometries it does not
+// cover; launch_step_tma runs it.
+constexpr size_t kPlanBytes = 512;
+bool plan_step_tma(const DevState& s, void* plan_out);
+size_t step_tma_plan_bytes();
+cudaError_t launch_step_tma(const DevState& s, const void* plan, int64_t g0, int64_t n,
+                            const float* q, const float* k, const float* v, float* out,
+                            cudaStream_t stream);
 
 // Bytes of f64 workspace the seal needs per group (key landmarks and every
 // head's query landmarks before rounding).

@@ -417,7 +417,7 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
   for (int p = tid; p < me * cw; p += kThreads) {
     const int i = p / cw, c = p - i * cw;
     tdst[(int64_t)i * dv + c] = ahi[i * kValTile + c];
-    ldst[(int64_t)i * dv + c] = (uint16_t)f32_to_bf16(alo[i * kValTile + c]);
+    ldst[(int64_t)i * dv + c] = (uint16_t)(pack_bf16x2(alo[i * kValTile + c], 0.f) & 0xffffu);
   }
 }
 

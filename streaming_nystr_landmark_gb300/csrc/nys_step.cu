@@ -323,8 +323,7 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
             if (cv) {
               float4 x = ld4(trow + 4 * c4);
               const uint2 lr = lrow[c4];
-              float4 lo = make_float4(bf16_to_f32(lr.x & 0xffffu), bf16_to_f32(lr.x >> 16),
-                                      bf16_to_f32(lr.y & 0xffffu), bf16_to_f32(lr.y >> 16));
+              float4 lo = make_float4(bf16_lo(lr.x), bf16_hi(lr.x), bf16_lo(lr.y), bf16_hi(lr.y));
               if (full) {
                 const float r = rs[hh * L.mp + b], e = es[hh * L.mp + b];
                 const float4 ve = ld4(vev + 4 * c4);
@@ -334,8 +333,8 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
                 comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
                 st4(trow + 4 * c4, x);
                 uint2 lw;
-                lw.x = f32_to_bf16(lo.x) | (f32_to_bf16(lo.y) << 16);
-                lw.y = f32_to_bf16(lo.z) | (f32_to_bf16(lo.w) << 16);
+                lw.x = pack_bf16x2(lo.x, lo.y);
+                lw.y = pack_bf16x2(lo.z, lo.w);
                 lrow[c4] = lw;
               }
               const float gb = gs[hh * L.mp + b];
@@ -399,6 +398,11 @@ cudaError_t launch_step(const DevState& s, int64_t g0, int64_t n,
                         const float* q, const float* k, const float* v,
                         float* out, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
+  // Geometries the persistent TMA kernel covers take it; the rest (H > 8,
+  // dv > 128, rows that are not 16-byte multiples) run the kernel below.
+  alignas(16) unsigned char plan[kPlanBytes];
+  if (step_tma_plan_bytes() <= sizeof(plan) && plan_step_tma(s, plan))
+    return launch_step_tma(s, plan, g0, n, q, k, v, out, stream);
   if (s.heads == 1) return launch_tile<1>(s, g0, n, q, k, v, out, stream);
   if (s.heads == 2) return launch_tile<2>(s, g0, n, q, k, v, out, stream);
   if (s.heads <= 4) return launch_tile<4>(s, g0, n, q, k, v, out, stream);

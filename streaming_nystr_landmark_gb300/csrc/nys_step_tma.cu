@@ -1,0 +1,732 @@
+// Persistent, TMA-fed decode step (the fast path of nys_step_batch).
+//
+// Same arithmetic as nys_step.cu -- nystrom.rs (docs.rs source view,
+// cortiq-engine 0.5.71), NystromState::advance, NystromHead::far_insert and
+// NystromHead::step -- reorganised for GB300's memory system.  The step is a
+// stream of ~300 KB per group with little arithmetic, so the kernel is built
+// around keeping HBM busy:
+//
+//  * one CTA per SM loops over groups; warp 8 is a producer whose lane 0
+//    streams every byte a group needs into a ring of 16 KB shared-memory
+//    stages with cp.async.bulk (the TMA bulk-copy engine), signalling each
+//    stage's arrival on an mbarrier with a transaction count;
+//  * warps 0..7 consume the stages in order and hand each one back through a
+//    second mbarrier, so the producer is always several stages -- and across
+//    group boundaries, the next group -- ahead;
+//  * per group the stages are: one "misc" stage (counters, queries, the new
+//    and the evicted key/value, running maxima, Z^), the K side (sink keys,
+//    window keys, key landmarks, each head's query landmarks, as one
+//    sequence of d-float rows), M, the V side (sink and window values), and
+//    T^ (hi and lo rows together).  Dot products of four rows x all heads are finished with one
+//    multi-value butterfly (4*HT values across 32 lanes in 4*HT - 1 shuffles).
+//
+// Every wait is bounded.  A wait that runs out sets a status word in the
+// group's ints slot kIntStatus and makes every warp leave; the producer then
+// waits (bounded) for its copies still in flight before the CTA exits.
+#include <cfloat>
+#include <cmath>
+
+#include "nys_internal.h"
+
+namespace nys {
+namespace {
+
+constexpr int kCWarps = 8;
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kThreadsTma = kCThreads + 32;
+constexpr int kStageBytes = 16384;
+constexpr int kMaxRing = 12;
+constexpr int kRowsPerRound = 4;
+constexpr uint64_t kWaitNs = 2000000000ull;  // every wait gives up after 2 s
+constexpr uint32_t kSuspendNs = 1000000;      // a waiting thread sleeps up to 1 ms per try
+constexpr int kSmemBudget = 227 * 1024;    // one CTA per SM
+constexpr int kSmemBudget2 = 113 * 1024;   // each of two CTAs per SM
+constexpr int kMinRing2 = 5;
+
+__host__ __device__ inline int r4(int x) { return (x + 3) & ~3; }
+
+// Where everything lives; computed once on the host, passed by value.
+struct TmaPlan {
+  int rows_k, rows_m, rows_v, rows_t;  // rows per stage of each stream
+  int tot_k;                           // w + m + H*m rows of d floats
+  int n_k, n_m, n_v, n_t, per_group;   // stages per group of each stream
+  // misc stage (bytes)
+  int mo_ints, mo_q, mo_knew, mo_vnew, mo_kev, mo_vev, mo_mmax, mo_zhi, mo_zlo;
+  int misc_bytes;
+  // consumer scratch (floats, after the ring)
+  int x_q, x_knew, x_vnew, x_kev, x_vev, x_mmax, x_zhi, x_zlo;
+  int x_sig, x_fh, x_lg, x_rs, x_es, x_gs, x_zs, x_ms, x_den, x_fl, x_ints, x_part;
+  int nrp, mp, scratch_floats;
+  int ring;
+  int ctas_per_sm;
+  int ring_off;  // bytes from the smem base to the ring
+  size_t smem_bytes;
+};
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t sptr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sptr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sptr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sptr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sptr(b)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(sptr(dst)),
+      "l"(src), "r"(bytes), "r"(sptr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// Sum each of V per-lane partials over the 32 lanes.  Returns, in every lane,
+// the total of value index reduce_index<V>(lane); lanes that share an index
+// hold the same total.
+template <int V>
+__device__ __forceinline__ float reduce_multi(float (&x)[V], int lane) {
+  constexpr int kSteps = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+#pragma unroll
+  for (int st = 0; st < kSteps; ++st) {
+    const int half = V >> (st + 1);
+    const int off = 16 >> st;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? x[i] : x[i + half];
+      const float keep = upper ? x[i + half] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = x[0];
+#pragma unroll
+  for (int off = 16 >> kSteps; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
+template <int V>
+__device__ __forceinline__ int reduce_index(int lane) {
+  constexpr int kSteps = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+  int v = 0;
+#pragma unroll
+  for (int st = 0; st < kSteps; ++st) v |= ((lane >> (4 - st)) & 1) << (kSteps - 1 - st);
+  return v;
+}
+template <int V>
+__device__ __forceinline__ bool reduce_writer(int lane) {
+  constexpr int kSteps = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+  return (lane & ((1 << (5 - kSteps)) - 1)) == 0;
+}
+
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false when 2 s passed or another warp gave up.
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort) {
+  if (mbar_test(b, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(b, parity)) return true;
+    if ((i & 15u) == 0u) {
+      if (abort && *abort) return false;
+      if (gtime() - t0 > kWaitNs) return false;
+    }
+  }
+}
+
+// -------------------------------------------------------------- kernel
+template <int HT>
+__global__ void __launch_bounds__(kThreadsTma, 2)
+step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __restrict__ q,
+                const float* __restrict__ k, const float* __restrict__ v,
+                float* __restrict__ out) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxRing;
+  uint64_t* cbar = empty + kMaxRing;
+  int* abort = reinterpret_cast<int*>(cbar + 1);
+  unsigned char* ring = smem + P.ring_off;
+  float* X = reinterpret_cast<float*>(ring + (size_t)P.ring * kStageBytes);
+
+  const int d = s.d, dv = s.dv, w = s.w, ns = s.sink, H = s.heads, m = s.m;
+  const int d4 = d >> 2, S = P.ring;
+
+  for (int i = tid; i < P.scratch_floats; i += blockDim.x) X[i] = 0.f;
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCWarps);
+    }
+    mbar_init(cbar, kCWarps);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ============================================================ producer
+  if (warp == kCWarps) {
+    if (lane != 0) return;
+    uint32_t c = 0;
+    bool ok = true;
+    for (int64_t gi = blockIdx.x; gi < n && ok; gi += gridDim.x) {
+      const int64_t g = g0 + gi;
+      const int32_t* ints = s.ints + g * kIntsPerGroup;
+      const int win_head = ints[kIntWinHead];
+      const int win_len = ints[kIntWinLen];
+      int slot = (win_len == w) ? win_head : win_len;
+      slot = min(max(slot, 0), w - 1);
+      for (int st = 0; st < P.per_group && ok; ++st, ++c) {
+        const int idx = (int)(c % (uint32_t)S);
+        if (!wait_bar(&empty[idx], ((c / S) & 1u) ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        unsigned char* dst = ring + (size_t)idx * kStageBytes;
+        uint64_t* bar = &full[idx];
+        if (st == 0) {
+          mbar_expect_tx(bar, (uint32_t)P.misc_bytes);
+          bulk_load(dst + P.mo_ints, ints, kIntsPerGroup * 4, bar);
+          bulk_load(dst + P.mo_q, q + gi * H * (int64_t)d, H * d * 4, bar);
+          bulk_load(dst + P.mo_knew, k + gi * (int64_t)d, d * 4, bar);
+          bulk_load(dst + P.mo_vnew, v + gi * (int64_t)dv, dv * 4, bar);
+          bulk_load(dst + P.mo_kev, s.win_k + (g * w + slot) * (int64_t)d, d * 4, bar);
+          bulk_load(dst + P.mo_vev, s.win_v + (g * w + slot) * (int64_t)dv, dv * 4, bar);
+          bulk_load(dst + P.mo_mmax, s.m_max + g * H * (int64_t)m, H * m * 4, bar);
+          bulk_load(dst + P.mo_zhi, s.z_hat + g * H * (int64_t)m, H * m * 4, bar);
+          bulk_load(dst + P.mo_zlo, s.z_lo + g * H * (int64_t)m, H * m * 4, bar);
+        } else if (st <= P.n_k) {
+          // K side: rows [r0, r1) of sink keys | window keys | key landmarks |
+          // Q~ (all heads), one row = d floats.
+          const int r0 = (st - 1) * P.rows_k;
+          const int r1 = min(r0 + P.rows_k, P.tot_k);
+          mbar_expect_tx(bar, (uint32_t)((r1 - r0) * d * 4));
+          const int seg[5] = {0, ns, ns + w, ns + w + m, P.tot_k};
+          const float* base[4] = {s.sink_k + g * ns * (int64_t)d, s.win_k + g * w * (int64_t)d,
+                                  s.k_tilde + g * m * (int64_t)d,
+                                  s.q_tilde + g * H * m * (int64_t)d};
+          for (int a = 0; a < 4; ++a) {
+            const int lo = max(r0, seg[a]), hi = min(r1, seg[a + 1]);
+            if (lo < hi)
+              bulk_load(dst + (size_t)(lo - r0) * d * 4, base[a] + (int64_t)(lo - seg[a]) * d,
+                        (uint32_t)((hi - lo) * d * 4), bar);
+          }
+        } else if (st <= P.n_k + P.n_m) {
+          const int r0 = (st - 1 - P.n_k) * P.rows_m;
+          const int r1 = min(r0 + P.rows_m, H * m);
+          mbar_expect_tx(bar, (uint32_t)((r1 - r0) * m * 4));
+          bulk_load(dst, s.mu + (g * H * m + r0) * (int64_t)m, (uint32_t)((r1 - r0) * m * 4), bar);
+        } else if (st <= P.n_k + P.n_m + P.n_v) {
+          // V side: rows [r0, r1) of sink values | window values.
+          const int r0 = (st - 1 - P.n_k - P.n_m) * P.rows_v;
+          const int r1 = min(r0 + P.rows_v, ns + w);
+          mbar_expect_tx(bar, (uint32_t)((r1 - r0) * dv * 4));
+          const int seg[3] = {0, ns, ns + w};
+          const float* base[2] = {s.sink_v + g * ns * (int64_t)dv, s.win_v + g * w * (int64_t)dv};
+          for (int a = 0; a < 2; ++a) {
+            const int lo = max(r0, seg[a]), hi = min(r1, seg[a + 1]);
+            if (lo < hi)
+              bulk_load(dst + (size_t)(lo - r0) * dv * 4, base[a] + (int64_t)(lo - seg[a]) * dv,
+                        (uint32_t)((hi - lo) * dv * 4), bar);
+          }
+        } else {
+          const int r0 = (st - 1 - P.n_k - P.n_m - P.n_v) * P.rows_t;
+          const int r1 = min(r0 + P.rows_t, H * m);
+          const uint32_t hb = (uint32_t)((r1 - r0) * dv * 4), lb = (uint32_t)((r1 - r0) * dv * 2);
+          mbar_expect_tx(bar, hb + lb);
+          bulk_load(dst, s.t_hat + (g * H * m + r0) * (int64_t)dv, hb, bar);
+          bulk_load(dst + (size_t)P.rows_t * dv * 4, s.t_lo + (g * H * m + r0) * (int64_t)dv, lb,
+                    bar);
+        }
+      }
+    }
+    if (!ok) {
+      atomicExch(abort, 1);
+      if (blockIdx.x < n) s.ints[(g0 + blockIdx.x) * kIntsPerGroup + kIntStatus] = 1;
+    }
+    // Whatever happened, no copy may still be landing in shared memory when
+    // the CTA exits: wait (bounded) for the last S stages issued.
+    const uint32_t first = c > (uint32_t)S ? c - (uint32_t)S : 0u;
+    for (uint32_t cc = first; cc < c; ++cc) wait_bar(&full[cc % S], (cc / S) & 1u, nullptr);
+    return;
+  }
+
+  // ============================================================ consumers
+  float* xq = X + P.x_q;
+  float* xknew = X + P.x_knew;
+  float* xvnew = X + P.x_vnew;
+  float* xkev = X + P.x_kev;
+  float* xvev = X + P.x_vev;
+  float* xmmax = X + P.x_mmax;
+  float* xzhi = X + P.x_zhi;
+  float* xzlo = X + P.x_zlo;
+  float* sig = X + P.x_sig;
+  float* fh = X + P.x_fh;
+  float* lg = X + P.x_lg;
+  float* rs = X + P.x_rs;
+  float* es = X + P.x_es;
+  float* gs = X + P.x_gs;
+  float* zs = X + P.x_zs;
+  float* ms = X + P.x_ms;
+  float* den = X + P.x_den;
+  int* xfl = reinterpret_cast<int*>(X + P.x_fl);
+  int* xints = reinterpret_cast<int*>(X + P.x_ints);
+  float* part = X + P.x_part;
+  const float scale = s.scale;
+  uint32_t c = 0;        // stage sequence number, as in the producer
+  uint32_t cphase = 0;   // consumer barrier phase
+  volatile int* vabort = abort;
+
+  auto release = [&](uint32_t cc) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[cc % S]);
+  };
+  auto acquire = [&](uint32_t cc) -> bool {
+    return wait_bar(&full[cc % S], (cc / S) & 1u, vabort);
+  };
+  auto csync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar);
+    const bool r = wait_bar(cbar, cphase, vabort);
+    cphase ^= 1u;
+    return r;
+  };
+  auto fail = [&](int64_t g) {
+    atomicExch(abort, 1);
+    s.ints[g * kIntsPerGroup + kIntStatus] = 1;
+  };
+
+  for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x) {
+    const int64_t g = g0 + gi;
+    // ---- misc stage: copy to scratch, hand the stage back at once.
+    if (!acquire(c)) { fail(g); return; }
+    {
+      const unsigned char* st = ring + (size_t)(c % S) * kStageBytes;
+      auto cp = [&](float* dst, int off, int nfl) {
+        const float* src = reinterpret_cast<const float*>(st + off);
+        for (int i = tid; i < (nfl >> 2); i += kCThreads) st4(dst + 4 * i, ld4(src + 4 * i));
+      };
+      cp(xq, P.mo_q, H * d);
+      cp(xknew, P.mo_knew, d);
+      cp(xvnew, P.mo_vnew, dv);
+      cp(xkev, P.mo_kev, d);
+      cp(xvev, P.mo_vev, dv);
+      cp(xmmax, P.mo_mmax, H * m);
+      cp(xzhi, P.mo_zhi, H * m);
+      cp(xzlo, P.mo_zlo, H * m);
+      if (tid < kIntsPerGroup) xints[tid] = reinterpret_cast<const int*>(st + P.mo_ints)[tid];
+      if (tid < H) xfl[tid] = s.far_len[g * H + tid];
+    }
+    release(c);
+    ++c;
+    if (!csync()) { fail(g); return; }
+    const int win_head = xints[kIntWinHead];
+    const int win_len = xints[kIntWinLen];
+    const int m_eff = min(max(xints[kIntMEff], 0), m);
+    const bool full = (win_len == w);
+    const int slot = full ? win_head : win_len;
+    const int nwin = full ? w : win_len + 1;
+    const int nnear = ns + nwin;
+    const bool ck = lane < d4;  // this lane's float4 column of a d-row
+    float4 qr[HT];
+#pragma unroll
+    for (int hh = 0; hh < HT; ++hh)
+      qr[hh] = ck ? ld4(xq + hh * d + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 kev4 = ck ? ld4(xkev + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    // ---- A: the K-side stages (sinks, window, key landmarks, Q~).
+    for (int st = 0; st < P.n_k; ++st, ++c) {
+      if (!acquire(c)) { fail(g); return; }
+      const float* stage = reinterpret_cast<const float*>(ring + (size_t)(c % S) * kStageBytes);
+      const int r0 = st * P.rows_k;
+      const int nrow = min(P.rows_k, P.tot_k - r0);
+      for (int base = 0; base < nrow; base += kCWarps * kRowsPerRound) {
+        float x[kRowsPerRound * HT];
+#pragma unroll
+        for (int i = 0; i < kRowsPerRound * HT; ++i) x[i] = 0.f;
+#pragma unroll
+        for (int u = 0; u < kRowsPerRound; ++u) {
+          const int lr = base + warp * kRowsPerRound + u;
+          if (lr < nrow) {
+            const int vr = r0 + lr;
+            const float* row = stage + (size_t)lr * d;
+            if (vr < ns + w + m) {
+              if (vr - ns == slot) row = xknew;
+              if (ck) {
+                const float4 a = ld4(row + 4 * lane);
+#pragma unroll
+                for (int hh = 0; hh < HT; ++hh) x[u * HT + hh] = dot4(a, qr[hh]);
+              }
+            } else if (ck) {
+              x[u * HT] = dot4(ld4(row + 4 * lane), kev4);
+            }
+          }
+        }
+        const float tot = reduce_multi<kRowsPerRound * HT>(x, lane);
+        if (reduce_writer<kRowsPerRound * HT>(lane)) {
+          const int vi = reduce_index<kRowsPerRound * HT>(lane);
+          const int u = vi / HT, hh = vi - u * HT;
+          const int lr = base + warp * kRowsPerRound + u;
+          if (lr < nrow) {
+            const int vr = r0 + lr;
+            const float l = tot * scale;
+            if (vr < ns + w) {
+              if (hh < H) sig[hh * P.nrp + vr] = l;
+            } else if (vr < ns + w + m) {
+              if (hh < H) fh[hh * P.mp + (vr - ns - w)] = l;
+            } else if (hh == 0) {
+              const int qr = vr - ns - w - m;
+              const int h = qr / m;
+              lg[h * P.mp + (qr - h * m)] = l;
+            }
+          }
+        }
+      }
+      release(c);
+    }
+    if (!csync()) { fail(g); return; }
+
+    // ---- B: per-head scalars with M from its stages.
+    const uint32_t c_m = c;
+    for (int i = 0; i < P.n_m; ++i)
+      if (!acquire(c_m + i)) { fail(g); return; }
+    for (int hh = warp; hh < H; hh += kCWarps) {
+      const int64_t hb = g * H + hh;
+      float* hfh = fh + hh * P.mp;
+      float* hgs = gs + hh * P.mp;
+      float* hzs = zs + hh * P.mp;
+      float* hms = ms + hh * P.mp;
+      float* hsig = sig + hh * P.nrp;
+      for (int i = lane; i < m_eff; i += 32) {
+        const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
+        float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
+        if (full) {
+          const float l = lg[hh * P.mp + i];
+          if (l > mo) {
+            r = expf(mo - l);
+            mn = l;
+          }
+          e = expf(l - mn);
+          comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
+          s.m_max[hb * m + i] = mn;
+          s.z_hat[hb * m + i] = zn;
+          s.z_lo[hb * m + i] = zln;
+        }
+        rs[hh * P.mp + i] = r;
+        es[hh * P.mp + i] = e;
+        hzs[i] = zn + zln;
+        hms[i] = mn;
+      }
+      const int fl_new = xfl[hh] + (full ? 1 : 0);
+      if (full && lane == 0) s.far_len[hb] = fl_new;
+      __syncwarp();
+      float cmax = -INFINITY;
+      for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
+      cmax = warp_max(cmax);
+      float c_all = cmax, far_den = 0.f;
+      if (fl_new > 0) {
+        float f = -INFINITY;
+        for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
+        f = warp_max(f);
+        for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
+        __syncwarp();
+        // This head's m x m block of M sits inside one stage (rows_m % m == 0).
+        const int mrow0 = hh * m;
+        const int msidx = mrow0 / P.rows_m;
+        const float* Mh = reinterpret_cast<const float*>(
+                              ring + (size_t)((c_m + msidx) % S) * kStageBytes) +
+                          (size_t)(mrow0 - msidx * P.rows_m) * m;
+        float cm = -INFINITY;
+        for (int b = lane; b < m_eff; b += 32) {
+          float u = 0.f;
+          for (int a = 0; a < m_eff; ++a) u = fmaf(hfh[a], Mh[a * m + b], u);
+          if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
+          hgs[b] = u;
+          cm = fmaxf(cm, f + hms[b]);
+        }
+        c_all = fmaxf(cmax, warp_max(cm));
+        float acc = 0.f;
+        for (int b = lane; b < m_eff; b += 32) {
+          const float gb = hgs[b] * expf(f + hms[b] - c_all);
+          hgs[b] = gb;
+          acc = fmaf(gb, hzs[b], acc);
+        }
+        far_den = warp_sum(acc);
+        if (!(far_den >= 0.f)) {
+          far_den = 0.f;
+          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+        }
+      } else {
+        for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+      }
+      float psum = 0.f;
+      for (int j = lane; j < nnear; j += 32) {
+        const float p = expf(hsig[j] - c_all);
+        hsig[j] = p;
+        psum += p;
+      }
+      psum = warp_sum(psum);
+      if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
+    }
+    for (int i = 0; i < P.n_m; ++i) release(c_m + i);
+    c += P.n_m;
+    if (!csync()) { fail(g); return; }
+
+    // ---- C: values and the far numerators.
+    const bool cv = lane < (dv >> 2);
+    float4 acc[HT];
+#pragma unroll
+    for (int hh = 0; hh < HT; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int st = 0; st < P.n_v; ++st, ++c) {
+      if (!acquire(c)) { fail(g); return; }
+      const float* stage = reinterpret_cast<const float*>(ring + (size_t)(c % S) * kStageBytes);
+      const int r0 = st * P.rows_v;
+      const int nrow = min(P.rows_v, ns + w - r0);
+      for (int lr = warp; lr < nrow; lr += kCWarps) {
+        const int j = r0 + lr;  // near row: sinks first, then window slots
+        if (j < nnear && cv) {
+          const float* row = (j - ns == slot) ? xvnew : stage + (size_t)lr * dv;
+          const float4 a = ld4(row + 4 * lane);
+#pragma unroll
+          for (int hh = 0; hh < HT; ++hh) {
+            const float p = (hh < H) ? sig[hh * P.nrp + j] : 0.f;
+            acc[hh].x = fmaf(p, a.x, acc[hh].x);
+            acc[hh].y = fmaf(p, a.y, acc[hh].y);
+            acc[hh].z = fmaf(p, a.z, acc[hh].z);
+            acc[hh].w = fmaf(p, a.w, acc[hh].w);
+          }
+        }
+      }
+      release(c);
+    }
+    const float4 ve = cv ? ld4(xvev + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int st = 0; st < P.n_t; ++st, ++c) {
+      if (!acquire(c)) { fail(g); return; }
+      const unsigned char* stage = ring + (size_t)(c % S) * kStageBytes;
+      const float* hi_rows = reinterpret_cast<const float*>(stage);
+      const uint16_t* lo_rows =
+          reinterpret_cast<const uint16_t*>(stage + (size_t)P.rows_t * dv * 4);
+      const int r0 = st * P.rows_t;
+      const int nrow = min(P.rows_t, H * m - r0);
+      for (int lr = warp; lr < nrow; lr += kCWarps) {
+        const int vr = r0 + lr;
+        const int h = vr / m, b = vr - h * m;
+        if (b < m_eff && cv) {
+          float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
+          const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
+          float4 lo = make_float4(bf16_lo(lr2.x), bf16_hi(lr2.x), bf16_lo(lr2.y), bf16_hi(lr2.y));
+          const int64_t grow = (g * H + h) * (int64_t)m + b;
+          if (full) {
+            const float r = rs[h * P.mp + b], e = es[h * P.mp + b];
+            comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
+            comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
+            comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
+            comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
+            st4(s.t_hat + grow * dv + 4 * lane, x);
+            uint2 lw;
+            lw.x = pack_bf16x2(lo.x, lo.y);
+            lw.y = pack_bf16x2(lo.z, lo.w);
+            *reinterpret_cast<uint2*>(s.t_lo + grow * dv + 4 * lane) = lw;
+          }
+          const float gb = gs[h * P.mp + b];
+#pragma unroll
+          for (int hh = 0; hh < HT; ++hh) {
+            if (hh == h) {
+              acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
+              acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
+              acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
+              acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
+            }
+          }
+        }
+      }
+      release(c);
+    }
+    // Cross-warp sum in two rounds through a buffer of kCWarps/2 slots.
+    constexpr int kHalf = kCWarps / 2;
+    if (warp >= kHalf && cv) {
+#pragma unroll
+      for (int hh = 0; hh < HT; ++hh)
+        st4(part + ((warp - kHalf) * HT + hh) * 128 + 4 * lane, acc[hh]);
+    }
+    if (!csync()) { fail(g); return; }
+    if (warp < kHalf && cv) {
+#pragma unroll
+      for (int hh = 0; hh < HT; ++hh) {
+        float* p = part + (warp * HT + hh) * 128 + 4 * lane;
+        const float4 o = ld4(p);
+        st4(p, make_float4(o.x + acc[hh].x, o.y + acc[hh].y, o.z + acc[hh].z, o.w + acc[hh].w));
+      }
+    }
+    if (!csync()) { fail(g); return; }
+    for (int idx = tid; idx < H * dv; idx += kCThreads) {
+      const int hh = idx / dv, col = idx - hh * dv;
+      float sum = 0.f;
+#pragma unroll
+      for (int wp = 0; wp < kHalf; ++wp) sum += part[(wp * HT + hh) * 128 + col];
+      out[(gi * H + hh) * (int64_t)dv + col] = sum / den[hh];
+    }
+    // The ring slot takes the new key/value; the counters move on.
+    for (int i = tid; i < d4; i += kCThreads)
+      st4(s.win_k + (g * w + slot) * (int64_t)d + 4 * i, ld4(xknew + 4 * i));
+    for (int i = tid; i < (dv >> 2); i += kCThreads)
+      st4(s.win_v + (g * w + slot) * (int64_t)dv + 4 * i, ld4(xvnew + 4 * i));
+    if (tid == 0) {
+      int32_t* ints = s.ints + g * kIntsPerGroup;
+      if (full) ints[kIntWinHead] = (win_head + 1) % w;
+      else ints[kIntWinLen] = win_len + 1;
+    }
+    if (!csync()) { fail(g); return; }
+  }
+}
+
+template <int HT>
+cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64_t n,
+                          const float* q, const float* k, const float* v, float* out,
+                          cudaStream_t stream) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      sms = 1;
+  }
+  cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)P.smem_bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t slots = (int64_t)sms * P.ctas_per_sm;
+  const int64_t grid = n < slots ? n : slots;
+  step_tma_kernel<HT><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(s, P, g0, n, q, k,
+                                                                          v, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Plan the stage layout; false when the geometry is outside this kernel
+// (every bulk copy must start and end on 16 bytes, dv <= 128, H <= 8, and the
+// misc stage and the scratch must fit).
+bool plan_step_tma(const DevState& s, void* plan_out) {
+  TmaPlan& P = *static_cast<TmaPlan*>(plan_out);
+  const int d = s.d, dv = s.dv, m = s.m, H = s.heads, w = s.w, ns = s.sink;
+  if (H > 8 || d > 128 || dv > 128 || (dv & 7) || (d & 3) || ((H * m) & 3) || (m & 3))
+    return false;
+  const int ht = H <= 1 ? 1 : H <= 2 ? 2 : H <= 4 ? 4 : 8;
+  P.rows_k = kStageBytes / (d * 4);
+  P.rows_m = kStageBytes / (m * 4);
+  if (P.rows_m % m) return false;  // a head's M block must not straddle stages
+  P.rows_v = kStageBytes / (dv * 4);
+  P.rows_t = kStageBytes / (dv * 6);
+  P.rows_t &= ~1;  // keeps the bf16 block 16-byte aligned for any dv % 8 == 0
+  if (P.rows_k < 1 || P.rows_m < 1 || P.rows_v < 1 || P.rows_t < 1) return false;
+  P.tot_k = ns + w + m + H * m;
+  P.n_k = (P.tot_k + P.rows_k - 1) / P.rows_k;
+  P.n_m = (H * m + P.rows_m - 1) / P.rows_m;
+  P.n_v = (ns + w + P.rows_v - 1) / P.rows_v;
+  P.n_t = (H * m + P.rows_t - 1) / P.rows_t;
+  P.per_group = 1 + P.n_k + P.n_m + P.n_v + P.n_t;
+  int o = 0;
+  P.mo_ints = o; o += kIntsPerGroup * 4;
+  P.mo_q = o;    o += H * d * 4;
+  P.mo_knew = o; o += d * 4;
+  P.mo_vnew = o; o += dv * 4;
+  P.mo_kev = o;  o += d * 4;
+  P.mo_vev = o;  o += dv * 4;
+  P.mo_mmax = o; o += H * m * 4;
+  P.mo_zhi = o;  o += H * m * 4;
+  P.mo_zlo = o;  o += H * m * 4;
+  P.misc_bytes = o;
+  if (o > kStageBytes) return false;
+  P.nrp = r4(ns + w);
+  P.mp = r4(m);
+  int x = 0;
+  P.x_q = x;    x += ht * d;
+  P.x_knew = x; x += d;
+  P.x_vnew = x; x += dv;
+  P.x_kev = x;  x += d;
+  P.x_vev = x;  x += dv;
+  P.x_mmax = x; x += H * m;
+  P.x_zhi = x;  x += H * m;
+  P.x_zlo = x;  x += H * m;
+  P.x_sig = x;  x += ht * P.nrp;
+  P.x_fh = x;   x += ht * P.mp;
+  P.x_lg = x;   x += ht * P.mp;
+  P.x_rs = x;   x += ht * P.mp;
+  P.x_es = x;   x += ht * P.mp;
+  P.x_gs = x;   x += ht * P.mp;
+  P.x_zs = x;   x += ht * P.mp;
+  P.x_ms = x;   x += ht * P.mp;
+  P.x_den = x;  x += r4(ht);
+  P.x_fl = x;   x += r4(ht);
+  P.x_ints = x; x += kIntsPerGroup;
+  P.x_part = x; x += (kCWarps / 2) * ht * 128;
+  P.scratch_floats = x;
+  P.ring_off = 1024;  // barriers and the abort flag live below
+  // M stays resident through the per-head phase; the ring must hold it plus
+  // room for the producer to keep going.  Two CTAs per SM when the ring still
+  // has kMinRing2 stages in half the shared memory, else one.
+  for (int per_sm = 2; per_sm >= 1; --per_sm) {
+    const long budget = per_sm == 2 ? kSmemBudget2 : kSmemBudget;
+    const long avail = budget - P.ring_off - (long)x * 4;
+    int ring = (int)(avail / kStageBytes);
+    if (ring > kMaxRing) ring = kMaxRing;
+    if (ring < P.n_m + 2 || (per_sm == 2 && ring < kMinRing2)) continue;
+    P.ring = ring;
+    P.ctas_per_sm = per_sm;
+    P.smem_bytes = (size_t)P.ring_off + (size_t)ring * kStageBytes + (size_t)x * 4;
+    return true;
+  }
+  return false;
+}
+
+size_t step_tma_plan_bytes() { return sizeof(TmaPlan); }
+
+cudaError_t launch_step_tma(const DevState& s, const void* plan, int64_t g0, int64_t n,
+                            const float* q, const float* k, const float* v, float* out,
+                            cudaStream_t stream) {
+  const TmaPlan& P = *static_cast<const TmaPlan*>(plan);
+  if (n <= 0) return cudaSuccess;
+  if (s.heads == 1) return launch_tma_ht<1>(s, P, g0, n, q, k, v, out, stream);
+  if (s.heads == 2) return launch_tma_ht<2>(s, P, g0, n, q, k, v, out, stream);
+  if (s.heads <= 4) return launch_tma_ht<4>(s, P, g0, n, q, k, v, out, stream);
+  return launch_tma_ht<8>(s, P, g0, n, q, k, v, out, stream);
+}
+
+}  // namespace nys

@@ -175,6 +175,7 @@ class ParityRun:
         assert np.all(far == ev), (far.min(), far.max(), ev)
         assert np.all(ints[:, 0] == (wl.t - wl.sink + self.n_steps) % wl.w)
         assert np.all(ints[:, 1] == wl.w)
+        assert np.all(ints[:, 5] == 0), "a decode kernel reported a timed-out wait"
 
     def close(self):
         self.st.close()
