@@ -35,7 +35,7 @@ METRIC = ("Nyström decode group-steps/s at batch 64, 28 layers; "
           "achieved HBM GB/s vs peak")
 UNIT = "group-steps/s"
 FALLBACK_HBM_GBS = 6800.0
-STEP_SOURCE = os.path.join(ROOT, "streaming_nystr_landmark_gb300", "csrc", "nys_step.cu")
+STEP_SOURCE = os.path.join(ROOT, "streaming_nystr_landmark_gb300", "csrc", "nys_step_tma.cu")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "step_kernel_batch64.txt")
 
 
@@ -344,7 +344,7 @@ def run_ours(args, wl):
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": per_launch,
-                "kernel": "step_kernel<2> (one launch per token)"}
+                "kernel": "step_tma_kernel<2> (one persistent launch per token)"}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         groups = [0, G // 2, G - 1]

@@ -203,18 +203,29 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   // ============================================================ producer
   if (warp == kCWarps) {
     if (lane != 0) return;
-    uint32_t c = 0;
+    uint32_t c = 0;        // stages issued so far
+    int idx = 0;           // c % S
+    uint32_t phase = 0;    // (c / S) & 1
     bool ok = true;
+    // The ring slot of the next group is read one group ahead so that the
+    // load's latency overlaps the current group's copies.
+    int2 nxt = make_int2(0, 0);
+    if (blockIdx.x < n) {
+      const int32_t* ints0 = s.ints + (g0 + blockIdx.x) * kIntsPerGroup;
+      nxt = make_int2(ints0[kIntWinHead], ints0[kIntWinLen]);
+    }
     for (int64_t gi = blockIdx.x; gi < n && ok; gi += gridDim.x) {
       const int64_t g = g0 + gi;
       const int32_t* ints = s.ints + g * kIntsPerGroup;
-      const int win_head = ints[kIntWinHead];
-      const int win_len = ints[kIntWinLen];
-      int slot = (win_len == w) ? win_head : win_len;
+      int slot = (nxt.y == w) ? nxt.x : nxt.y;
       slot = min(max(slot, 0), w - 1);
-      for (int st = 0; st < P.per_group && ok; ++st, ++c) {
-        const int idx = (int)(c % (uint32_t)S);
-        if (!wait_bar(&empty[idx], ((c / S) & 1u) ^ 1u, abort)) {
+      if (gi + gridDim.x < n) {
+        const int32_t* in2 = s.ints + (g + gridDim.x) * kIntsPerGroup;
+        nxt = make_int2(in2[kIntWinHead], in2[kIntWinLen]);
+      }
+      for (int st = 0; st < P.per_group && ok;
+           ++st, ++c, idx = (idx + 1 == S) ? 0 : idx + 1, phase ^= (idx == 0) ? 1u : 0u) {
+        if (!wait_bar(&empty[idx], phase ^ 1u, abort)) {
           ok = false;
           break;
         }
@@ -284,7 +295,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     // the CTA exits: wait (bounded) for the last S stages issued.
     const uint32_t first = c > (uint32_t)S ? c - (uint32_t)S : 0u;
     for (uint32_t cc = first; cc < c; ++cc) wait_bar(&full[cc % S], (cc / S) & 1u, nullptr);
-    return;
+    return;  // (the division above runs once, at exit)
   }
 
   // ============================================================ consumers
@@ -305,20 +316,28 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   float* zs = X + P.x_zs;
   float* ms = X + P.x_ms;
   float* den = X + P.x_den;
-  int* xfl = reinterpret_cast<int*>(X + P.x_fl);
   int* xints = reinterpret_cast<int*>(X + P.x_ints);
   float* part = X + P.x_part;
   const float scale = s.scale;
-  uint32_t c = 0;        // stage sequence number, as in the producer
+  // Ring cursor of the next stage to consume: slot index and phase parity,
+  // advanced incrementally (no division by the ring length).
+  int ci = 0;
+  uint32_t cpar = 0;
   uint32_t cphase = 0;   // consumer barrier phase
   volatile int* vabort = abort;
-
-  auto release = [&](uint32_t cc) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[cc % S]);
+  auto advance = [&]() {
+    if (++ci == S) {
+      ci = 0;
+      cpar ^= 1u;
+    }
   };
-  auto acquire = [&](uint32_t cc) -> bool {
-    return wait_bar(&full[cc % S], (cc / S) & 1u, vabort);
+  auto stage_ptr = [&](int i) { return ring + (size_t)i * kStageBytes; };
+  auto release_slot = [&](int i) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[i]);
+  };
+  auto acquire_slot = [&](int i, uint32_t par) -> bool {
+    return wait_bar(&full[i], par, vabort);
   };
   auto csync = [&]() -> bool {
     __syncwarp();
@@ -334,10 +353,13 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
 
   for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x) {
     const int64_t g = g0 + gi;
+    // far_len of the head this warp owns in the per-head phase; loaded now so
+    // that its latency hides behind the K side.
+    const int fl_old = (warp < H && lane == 0) ? s.far_len[g * H + warp] : 0;
     // ---- misc stage: copy to scratch, hand the stage back at once.
-    if (!acquire(c)) { fail(g); return; }
+    if (!acquire_slot(ci, cpar)) { fail(g); return; }
     {
-      const unsigned char* st = ring + (size_t)(c % S) * kStageBytes;
+      const unsigned char* st = stage_ptr(ci);
       auto cp = [&](float* dst, int off, int nfl) {
         const float* src = reinterpret_cast<const float*>(st + off);
         for (int i = tid; i < (nfl >> 2); i += kCThreads) st4(dst + 4 * i, ld4(src + 4 * i));
@@ -351,10 +373,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       cp(xzhi, P.mo_zhi, H * m);
       cp(xzlo, P.mo_zlo, H * m);
       if (tid < kIntsPerGroup) xints[tid] = reinterpret_cast<const int*>(st + P.mo_ints)[tid];
-      if (tid < H) xfl[tid] = s.far_len[g * H + tid];
     }
-    release(c);
-    ++c;
+    release_slot(ci);
+    advance();
     if (!csync()) { fail(g); return; }
     const int win_head = xints[kIntWinHead];
     const int win_len = xints[kIntWinLen];
@@ -371,9 +392,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     const float4 kev4 = ck ? ld4(xkev + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // ---- A: the K-side stages (sinks, window, key landmarks, Q~).
-    for (int st = 0; st < P.n_k; ++st, ++c) {
-      if (!acquire(c)) { fail(g); return; }
-      const float* stage = reinterpret_cast<const float*>(ring + (size_t)(c % S) * kStageBytes);
+    for (int st = 0; st < P.n_k; ++st, advance()) {
+      if (!acquire_slot(ci, cpar)) { fail(g); return; }
+      const float* stage = reinterpret_cast<const float*>(stage_ptr(ci));
       const int r0 = st * P.rows_k;
       const int nrow = min(P.rows_k, P.tot_k - r0);
       for (int base = 0; base < nrow; base += kCWarps * kRowsPerRound) {
@@ -411,21 +432,34 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             } else if (vr < ns + w + m) {
               if (hh < H) fh[hh * P.mp + (vr - ns - w)] = l;
             } else if (hh == 0) {
-              const int qr = vr - ns - w - m;
-              const int h = qr / m;
-              lg[h * P.mp + (qr - h * m)] = l;
+              int qr = vr - ns - w - m;
+              int h = 0;
+              while (qr >= m) {  // at most H - 1 steps
+                qr -= m;
+                ++h;
+              }
+              lg[h * P.mp + qr] = l;
             }
           }
         }
       }
-      release(c);
+      release_slot(ci);
     }
     if (!csync()) { fail(g); return; }
 
     // ---- B: per-head scalars with M from its stages.
-    const uint32_t c_m = c;
-    for (int i = 0; i < P.n_m; ++i)
-      if (!acquire(c_m + i)) { fail(g); return; }
+    const int ci_m = ci;
+    {
+      int i2 = ci;
+      uint32_t p2 = cpar;
+      for (int i = 0; i < P.n_m; ++i) {
+        if (!acquire_slot(i2, p2)) { fail(g); return; }
+        if (++i2 == S) {
+          i2 = 0;
+          p2 ^= 1u;
+        }
+      }
+    }
     for (int hh = warp; hh < H; hh += kCWarps) {
       const int64_t hb = g * H + hh;
       float* hfh = fh + hh * P.mp;
@@ -453,7 +487,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         hzs[i] = zn + zln;
         hms[i] = mn;
       }
-      const int fl_new = xfl[hh] + (full ? 1 : 0);
+      const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
       if (full && lane == 0) s.far_len[hb] = fl_new;
       __syncwarp();
       float cmax = -INFINITY;
@@ -467,11 +501,12 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
         __syncwarp();
         // This head's m x m block of M sits inside one stage (rows_m % m == 0).
-        const int mrow0 = hh * m;
-        const int msidx = mrow0 / P.rows_m;
-        const float* Mh = reinterpret_cast<const float*>(
-                              ring + (size_t)((c_m + msidx) % S) * kStageBytes) +
-                          (size_t)(mrow0 - msidx * P.rows_m) * m;
+        int mrow0 = hh * m, mslot = ci_m;
+        while (mrow0 >= P.rows_m) {  // at most n_m - 1 steps
+          mrow0 -= P.rows_m;
+          if (++mslot == S) mslot = 0;
+        }
+        const float* Mh = reinterpret_cast<const float*>(stage_ptr(mslot)) + (size_t)mrow0 * m;
         float cm = -INFINITY;
         for (int b = lane; b < m_eff; b += 32) {
           float u = 0.f;
@@ -504,8 +539,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       psum = warp_sum(psum);
       if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
     }
-    for (int i = 0; i < P.n_m; ++i) release(c_m + i);
-    c += P.n_m;
+    for (int i = 0; i < P.n_m; ++i) {
+      release_slot(ci);
+      advance();
+    }
     if (!csync()) { fail(g); return; }
 
     // ---- C: values and the far numerators.
@@ -513,9 +550,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     float4 acc[HT];
 #pragma unroll
     for (int hh = 0; hh < HT; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int st = 0; st < P.n_v; ++st, ++c) {
-      if (!acquire(c)) { fail(g); return; }
-      const float* stage = reinterpret_cast<const float*>(ring + (size_t)(c % S) * kStageBytes);
+    for (int st = 0; st < P.n_v; ++st, advance()) {
+      if (!acquire_slot(ci, cpar)) { fail(g); return; }
+      const float* stage = reinterpret_cast<const float*>(stage_ptr(ci));
       const int r0 = st * P.rows_v;
       const int nrow = min(P.rows_v, ns + w - r0);
       for (int lr = warp; lr < nrow; lr += kCWarps) {
@@ -533,20 +570,37 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           }
         }
       }
-      release(c);
+      release_slot(ci);
     }
     const float4 ve = cv ? ld4(xvev + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int st = 0; st < P.n_t; ++st, ++c) {
-      if (!acquire(c)) { fail(g); return; }
-      const unsigned char* stage = ring + (size_t)(c % S) * kStageBytes;
+    // (head, landmark) of T^ rows, stepped without dividing by m: (sh, sb) is
+    // the current stage's first row, (th, tb) this warp's next row.
+    int sh = 0, sb = 0;
+    for (int st = 0; st < P.n_t; ++st, advance()) {
+      if (!acquire_slot(ci, cpar)) { fail(g); return; }
+      const unsigned char* stage = stage_ptr(ci);
+      int th = sh, tb = sb + warp;
+      while (tb >= m) {
+        tb -= m;
+        ++th;
+      }
+      sb += P.rows_t;
+      while (sb >= m) {
+        sb -= m;
+        ++sh;
+      }
       const float* hi_rows = reinterpret_cast<const float*>(stage);
       const uint16_t* lo_rows =
           reinterpret_cast<const uint16_t*>(stage + (size_t)P.rows_t * dv * 4);
       const int r0 = st * P.rows_t;
       const int nrow = min(P.rows_t, H * m - r0);
       for (int lr = warp; lr < nrow; lr += kCWarps) {
-        const int vr = r0 + lr;
-        const int h = vr / m, b = vr - h * m;
+        const int h = th, b = tb;
+        tb += kCWarps;
+        while (tb >= m) {
+          tb -= m;
+          ++th;
+        }
         if (b < m_eff && cv) {
           float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
           const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
@@ -576,7 +630,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           }
         }
       }
-      release(c);
+      release_slot(ci);
     }
     // Cross-warp sum in two rounds through a buffer of kCWarps/2 slots.
     constexpr int kHalf = kCWarps / 2;
