@@ -276,41 +276,50 @@ pinv_kernel(DevState s, int64_t g0, int m_eff, const double* __restrict__ ws) {
 }
 
 // ---------------------------------------------------------------- 3
-constexpr int kKeyBlock = 32;
-constexpr int kValTile = 128;  // value columns per block (grid.y tiles dv)
+// One block per (group, head, 128-column value tile): 16 x 16 threads, thread
+// (ty, tx) owns landmark rows ty*TR .. ty*TR+TR-1.  Keys are consumed in
+// blocks of kKeyBlock = 64:
+//   logits  L[TR][4] for keys tx*4..tx*4+3 from Q~^T and K^T in shared memory
+//           (one float4 of each feeds 4*TR FMAs);
+//   online  per-row block maximum over the 16 lanes of the row group, new
+//   max     running maximum, rescale alpha = exp(old - new), p = exp(L - max);
+//   values  the block's p (reusing the key tile's shared memory, transposed)
+//           times the value tile: part[TR][8] for columns tx*8..tx*8+7;
+//   fold    (hi, lo) <- (hi, lo) * alpha + part, compensated (comp_axpy), so
+//           that tens of thousands of keys do not accumulate f32 rounding.
+constexpr int kKeyBlock = 64;
+constexpr int kValTile = 128;
+constexpr int kKtStride = kKeyBlock + 4;  // 68: conflict-free transposed stores
 
-struct ReplaySmem {
-  int qt, kb, vb, p, hi, lo, rmax, zhi, zlo, alpha, total, dp, pp;
-  __host__ __device__ ReplaySmem(int me, int d) {
-    dp = d + 4;  // skewed rows: float4 reads across lanes hit all banks
-    pp = kKeyBlock + 1;
-    const int m4 = (me + 3) & ~3;
-    int o = 0;
-    qt = o;    o += me * dp;
-    kb = o;    o += kKeyBlock * dp;
-    vb = o;    o += kKeyBlock * kValTile;
-    p = o;     o += ((me * pp + 3) & ~3);
-    hi = o;    o += me * kValTile;
-    lo = o;    o += me * kValTile;
-    rmax = o;  o += m4;
-    zhi = o;   o += m4;
-    zlo = o;   o += m4;
-    alpha = o; o += m4;
-    total = o;
+// The key tile and, after the logits, the probability tile share one region.
+__host__ __device__ inline size_t replay_kt_floats(int rt, int d) {
+  const size_t a = (size_t)d * kKtStride, b = (size_t)kKeyBlock * rt;
+  return a > b ? a : b;
+}
+__host__ __device__ inline size_t replay_smem_floats(int rt, int d) {
+  return (size_t)d * rt + replay_kt_floats(rt, d) + (size_t)kKeyBlock * kValTile;
+}
+
+template <int TR>
+__device__ __forceinline__ void load_rows(const float* p, float (&a)[TR]) {
+  if constexpr (TR == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+  } else if constexpr (TR == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(p);
+    a[0] = x.x; a[1] = x.y;
+  } else {
+    a[0] = p[0];
   }
-};
+}
 
-// One block per (group, head, value tile).  Keys are consumed in blocks of
-// kKeyBlock: logits L = Q~ K_blk^T * scale, a per-landmark online maximum,
-// block sums of exp(L - max) and of exp(L - max) v, and a compensated fold of
-// each block sum into the running (hi, lo) accumulators.  Every value tile
-// recomputes the same logits, so the tile with blockIdx.y == 0 alone writes
-// m_max and Z^.
-__global__ void __launch_bounds__(kThreads)
+template <int TR>
+__global__ void __launch_bounds__(kThreads, 2)
 replay_kernel(DevState s, int64_t g0, int t, int m_eff,
               const float* __restrict__ k, const float* __restrict__ v) {
+  constexpr int RT = 16 * TR;
   extern __shared__ __align__(16) float fsm[];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int H = s.heads, m = s.m, d = s.d, dv = s.dv, w = s.w, ns = s.sink;
   const int d4 = d >> 2, me = m_eff;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
@@ -318,107 +327,182 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
   const int64_t hb = g * H + h;
   const int c0 = blockIdx.y * kValTile;
   const int cw = min(kValTile, dv - c0);
-  const int cw4 = cw >> 2;
   const float scale = s.scale;
-  const ReplaySmem L(me, d);
-  float* qt = fsm + L.qt;
-  float* kb = fsm + L.kb;
-  float* vb = fsm + L.vb;
-  float* P = fsm + L.p;
-  float* ahi = fsm + L.hi;
-  float* alo = fsm + L.lo;
-  float* rmax = fsm + L.rmax;
-  float* zhi = fsm + L.zhi;
-  float* zlo = fsm + L.zlo;
-  float* alpha = fsm + L.alpha;
+  float* QT = fsm;                     // [d][RT]   Q~ transposed, rows >= m_eff zero
+  float* KT = QT + (size_t)d * RT;     // [d][kKtStride]  key block transposed
+  float* PT = KT;                      // [kKeyBlock][RT] p, after the logits
+  float* VB = KT + replay_kt_floats(RT, d);  // [kKeyBlock][kValTile]
 
   const float* qsrc = s.q_tilde + hb * m * (int64_t)d;
-  for (int idx = tid; idx < me * d4; idx += kThreads) {
-    const int i = idx / d4, c = idx - i * d4;
-    st4(qt + i * L.dp + 4 * c, ld4(qsrc + (int64_t)i * d + 4 * c));
+  for (int idx = tid; idx < RT * d; idx += kThreads) {
+    const int i = idx / d, c = idx - i * d;
+    QT[c * RT + i] = i < me ? qsrc[(int64_t)i * d + c] : 0.f;
   }
-  for (int i = tid; i < me; i += kThreads) {
-    rmax[i] = -INFINITY;
-    zhi[i] = 0.f;
-    zlo[i] = 0.f;
-  }
-  for (int idx = tid; idx < me * kValTile; idx += kThreads) {
-    ahi[idx] = 0.f;
-    alo[idx] = 0.f;
+
+  float hi[TR][8], lo[TR][8], mrow[TR], zh[TR], zl[TR];
+#pragma unroll
+  for (int i = 0; i < TR; ++i) {
+    mrow[i] = -INFINITY;
+    zh[i] = 0.f;
+    zl[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      hi[i][c] = 0.f;
+      lo[i][c] = 0.f;
+    }
   }
 
   const float* ksrc = k + gi * (int64_t)t * d;
   const float* vsrc = v + gi * (int64_t)t * dv + c0;
   const int j_end = t - w;  // keys sink .. t-w-1 were evicted by the replay
+  const int klane = tid & 15, kchunk = tid >> 4;  // 16 keys x 16 chunk lanes
   for (int j0 = ns; j0 < j_end; j0 += kKeyBlock) {
     const int nb = min(kKeyBlock, j_end - j0);
-    for (int idx = tid; idx < nb * d4; idx += kThreads) {
-      const int jj = idx / d4, c = idx - jj * d4;
-      st4(kb + jj * L.dp + 4 * c, ld4(ksrc + (int64_t)(j0 + jj) * d + 4 * c));
-    }
-    for (int idx = tid; idx < nb * cw4; idx += kThreads) {
-      const int jj = idx / cw4, c = idx - jj * cw4;
-      st4(vb + jj * kValTile + 4 * c, ld4(vsrc + (int64_t)(j0 + jj) * dv + 4 * c));
-    }
-    __syncthreads();
-    for (int p = tid; p < me * nb; p += kThreads) {
-      const int i = p / nb, jj = p - i * nb;
-      const float* a = qt + i * L.dp;
-      const float* b = kb + jj * L.dp;
-      float x = 0.f;
-      for (int c = 0; c < d4; ++c) {
-        const float4 qa = ld4(a + 4 * c), kk = ld4(b + 4 * c);
-        x += qa.x * kk.x + qa.y * kk.y + qa.z * kk.z + qa.w * kk.w;
+    __syncthreads();  // the previous block is done with KT / PT / VB
+    // Keys, transposed: thread (klane, kchunk) moves float4 chunks
+    // kchunk, kchunk + 16, ... of keys klane, klane + 16, ...
+    for (int kk = klane; kk < kKeyBlock; kk += 16) {
+      const bool valid = kk < nb;
+      const float* row = ksrc + (int64_t)(j0 + kk) * d;
+      for (int c4 = kchunk; c4 < d4; c4 += 16) {
+        const float4 x = valid ? *reinterpret_cast<const float4*>(row + 4 * c4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        KT[(4 * c4 + 0) * kKtStride + kk] = x.x;
+        KT[(4 * c4 + 1) * kKtStride + kk] = x.y;
+        KT[(4 * c4 + 2) * kKtStride + kk] = x.z;
+        KT[(4 * c4 + 3) * kKtStride + kk] = x.w;
       }
-      P[i * L.pp + jj] = x * scale;
+    }
+    // Values of this column tile; rows past the block are zero.
+    const int cw4 = cw >> 2;
+    for (int idx = tid; idx < kKeyBlock * (kValTile / 4); idx += kThreads) {
+      const int jj = idx >> 5, c4 = idx & 31;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (jj < nb && c4 < cw4)
+        x = *reinterpret_cast<const float4*>(vsrc + (int64_t)(j0 + jj) * dv + 4 * c4);
+      *reinterpret_cast<float4*>(VB + jj * kValTile + 4 * c4) = x;
     }
     __syncthreads();
-    for (int i = tid; i < me; i += kThreads) {
+
+    float L[TR][4];
+#pragma unroll
+    for (int i = 0; i < TR; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) L[i][j] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < d; ++c) {
+      float a[TR];
+      load_rows<TR>(QT + c * RT + ty * TR, a);
+      const float4 b = *reinterpret_cast<const float4*>(KT + c * kKtStride + tx * 4);
+#pragma unroll
+      for (int i = 0; i < TR; ++i) {
+        L[i][0] = fmaf(a[i], b.x, L[i][0]);
+        L[i][1] = fmaf(a[i], b.y, L[i][1]);
+        L[i][2] = fmaf(a[i], b.z, L[i][2]);
+        L[i][3] = fmaf(a[i], b.w, L[i][3]);
+      }
+    }
+    float alpha[TR];
+#pragma unroll
+    for (int i = 0; i < TR; ++i) {
       float bm = -INFINITY;
-      for (int jj = 0; jj < nb; ++jj) bm = fmaxf(bm, P[i * L.pp + jj]);
-      const float old = rmax[i];
-      const float nm = fmaxf(old, bm);
-      const float a = (old == -INFINITY) ? 0.f : expf(old - nm);
-      float zb = 0.f;
-      for (int jj = 0; jj < nb; ++jj) {
-        const float e = expf(P[i * L.pp + jj] - nm);
-        P[i * L.pp + jj] = e;
-        zb += e;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        L[i][j] = (tx * 4 + j < nb) ? L[i][j] * scale : -INFINITY;
+        bm = fmaxf(bm, L[i][j]);
       }
+#pragma unroll
+      for (int o = 8; o; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      const float nm = fmaxf(mrow[i], bm);
+      alpha[i] = (mrow[i] == -INFINITY) ? 0.f : expf(mrow[i] - nm);
+      mrow[i] = nm;
+      float zb = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        L[i][j] = (tx * 4 + j < nb) ? expf(L[i][j] - nm) : 0.f;
+        zb += L[i][j];
+      }
+#pragma unroll
+      for (int o = 8; o; o >>= 1) zb += __shfl_xor_sync(0xffffffffu, zb, o);
       float nh, nl;
-      comp_axpy(zhi[i], zlo[i], a, zb, 1.f, nh, nl);
-      zhi[i] = nh;
-      zlo[i] = nl;
-      rmax[i] = nm;
-      alpha[i] = a;
+      comp_axpy(zh[i], zl[i], alpha[i], zb, 1.f, nh, nl);
+      zh[i] = nh;
+      zl[i] = nl;
     }
+    __syncthreads();  // every thread is done reading KT: p takes its place
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < TR; ++i) PT[(tx * 4 + j) * RT + ty * TR + i] = L[i][j];
     __syncthreads();
-    for (int p = tid; p < me * cw; p += kThreads) {
-      const int i = p / cw, c = p - i * cw;
-      float part = 0.f;
-      for (int jj = 0; jj < nb; ++jj) part = fmaf(P[i * L.pp + jj], vb[jj * kValTile + c], part);
-      float nh, nl;
-      comp_axpy(ahi[i * kValTile + c], alo[i * kValTile + c], alpha[i], part, 1.f, nh, nl);
-      ahi[i * kValTile + c] = nh;
-      alo[i * kValTile + c] = nl;
+
+    float part[TR][8];
+#pragma unroll
+    for (int i = 0; i < TR; ++i)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) part[i][c] = 0.f;
+#pragma unroll 4
+    for (int jj = 0; jj < kKeyBlock; ++jj) {
+      float a[TR];
+      load_rows<TR>(PT + jj * RT + ty * TR, a);
+      const float4 b0 = *reinterpret_cast<const float4*>(VB + jj * kValTile + tx * 8);
+      const float4 b1 = *reinterpret_cast<const float4*>(VB + jj * kValTile + tx * 8 + 4);
+#pragma unroll
+      for (int i = 0; i < TR; ++i) {
+        part[i][0] = fmaf(a[i], b0.x, part[i][0]);
+        part[i][1] = fmaf(a[i], b0.y, part[i][1]);
+        part[i][2] = fmaf(a[i], b0.z, part[i][2]);
+        part[i][3] = fmaf(a[i], b0.w, part[i][3]);
+        part[i][4] = fmaf(a[i], b1.x, part[i][4]);
+        part[i][5] = fmaf(a[i], b1.y, part[i][5]);
+        part[i][6] = fmaf(a[i], b1.z, part[i][6]);
+        part[i][7] = fmaf(a[i], b1.w, part[i][7]);
+      }
     }
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < TR; ++i)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float nh, nl;
+        comp_axpy(hi[i][c], lo[i][c], alpha[i], part[i][c], 1.f, nh, nl);
+        hi[i][c] = nh;
+        lo[i][c] = nl;
+      }
   }
 
-  if (blockIdx.y == 0) {
-    for (int i = tid; i < me; i += kThreads) {
-      s.m_max[hb * m + i] = rmax[i];
-      s.z_hat[hb * m + i] = zhi[i];
-      s.z_lo[hb * m + i] = zlo[i];
+#pragma unroll
+  for (int i = 0; i < TR; ++i) {
+    const int row = ty * TR + i;
+    if (row >= me) continue;
+    if (blockIdx.y == 0 && tx == 0) {
+      s.m_max[hb * m + row] = mrow[i];
+      s.z_hat[hb * m + row] = zh[i];
+      s.z_lo[hb * m + row] = zl[i];
+    }
+    float* tdst = s.t_hat + (hb * m + row) * (int64_t)dv + c0;
+    uint16_t* ldst = s.t_lo + (hb * m + row) * (int64_t)dv + c0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int col = tx * 8 + c;
+      if (col < cw) {
+        tdst[col] = hi[i][c];
+        ldst[col] = (uint16_t)(pack_bf16x2(lo[i][c], 0.f) & 0xffffu);
+      }
     }
   }
-  float* tdst = s.t_hat + hb * m * (int64_t)dv + c0;
-  uint16_t* ldst = s.t_lo + hb * m * (int64_t)dv + c0;
-  for (int p = tid; p < me * cw; p += kThreads) {
-    const int i = p / cw, c = p - i * cw;
-    tdst[(int64_t)i * dv + c] = ahi[i * kValTile + c];
-    ldst[(int64_t)i * dv + c] = (uint16_t)(pack_bf16x2(alo[i * kValTile + c], 0.f) & 0xffffu);
-  }
+}
+
+template <int TR>
+cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, int t, int m_eff,
+                          const float* k, const float* v, cudaStream_t stream) {
+  const size_t bytes = replay_smem_floats(16 * TR, s.d) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(replay_kernel<TR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
+  replay_kernel<TR><<<dim3((unsigned)(n * s.heads), tiles), kThreads, bytes, stream>>>(
+      s, g0, t, m_eff, k, v);
+  return cudaGetLastError();
 }
 
 cudaError_t set_smem(const void* fn, size_t bytes) {
@@ -447,13 +531,9 @@ cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
   pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, m_eff, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const ReplaySmem R(m_eff, s.d);
-  const size_t rbytes = (size_t)R.total * sizeof(float);
-  if ((e = set_smem((const void*)replay_kernel, rbytes)) != cudaSuccess) return e;
-  const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
-  replay_kernel<<<dim3((unsigned)(n * s.heads), tiles), kThreads, rbytes, stream>>>(
-      s, g0, t, m_eff, k, v);
-  return cudaGetLastError();
+  if (m_eff <= 16) return launch_replay<1>(s, g0, n, t, m_eff, k, v, stream);
+  if (m_eff <= 32) return launch_replay<2>(s, g0, n, t, m_eff, k, v, stream);
+  return launch_replay<4>(s, g0, n, t, m_eff, k, v, stream);
 }
 
 }  // namespace nys
