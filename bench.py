@@ -165,6 +165,13 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate_rate(world, groups_per_rank, steps, seconds):
+    """Whole-job group-steps/s: every rank steps its own replica of the
+    workload, and the job takes as long as its slowest rank (`seconds` is the
+    max over ranks)."""
+    return world * groups_per_rank * steps / seconds
+
+
 def max_over_ranks(x, world, device):
     if world == 1:
         return x
@@ -297,7 +304,7 @@ def run_ours(args, wl):
     barrier(world)
     clk = clocks.stop()
     dt = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
-    value = world * G * args.steps / dt
+    value = aggregate_rate(world, G, args.steps, dt)
     launch_s = dt / args.steps
     finite = bool(torch.isfinite(out).all().item())
     del tq, tk, tv
@@ -329,7 +336,7 @@ def run_ours(args, wl):
     torch.cuda.synchronize(dev)
     barrier(world)
     dt_e2e = max_over_ranks(e2.elapsed_time(e3) / 1e3, world, dev)
-    e2e = {"value": world * G * e2e_steps / dt_e2e, "unit": UNIT,
+    e2e = {"value": aggregate_rate(world, G, e2e_steps, dt_e2e), "unit": UNIT,
            "h2d_bytes_per_step": 4 * G * (H * wl.d + wl.d + wl.dv),
            "d2h_bytes_per_step": 4 * G * H * wl.dv}
     st.close()
