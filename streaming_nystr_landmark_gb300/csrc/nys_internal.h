@@ -78,6 +78,48 @@ __device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, 
   nlo = t - (nhi - s);
 }
 
+// Compensated dot product (Ogita, Rump and Oishi's Dot2): sum_a x[a] * y[a*ys]
+// with each product's rounding error recovered by FMA and each addition's by
+// two-sum, so the result is as accurate as if accumulated in twice the
+// precision.  The mixing row u = F^ M is a sum with heavy cancellation (M is
+// the ridge pseudo-inverse of an ill-conditioned kernel matrix), and plain
+// f32 accumulation there costs up to ~1e-4 of output accuracy at m = 64.
+// Two interleaved chains shorten the dependency chain.
+__device__ __forceinline__ float dot2(const float* x, const float* y, int ys, int n) {
+  float s0 = 0.f, c0 = 0.f, s1 = 0.f, c1 = 0.f;
+  int a = 0;
+  for (; a + 2 <= n; a += 2) {
+    {
+      const float h = x[a] * y[a * ys];
+      const float r = fmaf(x[a], y[a * ys], -h);
+      const float t = s0 + h;
+      const float z = t - s0;
+      c0 += ((s0 - (t - z)) + (h - z)) + r;
+      s0 = t;
+    }
+    {
+      const float h = x[a + 1] * y[(a + 1) * ys];
+      const float r = fmaf(x[a + 1], y[(a + 1) * ys], -h);
+      const float t = s1 + h;
+      const float z = t - s1;
+      c1 += ((s1 - (t - z)) + (h - z)) + r;
+      s1 = t;
+    }
+  }
+  if (a < n) {
+    const float h = x[a] * y[a * ys];
+    const float r = fmaf(x[a], y[a * ys], -h);
+    const float t = s0 + h;
+    const float z = t - s0;
+    c0 += ((s0 - (t - z)) + (h - z)) + r;
+    s0 = t;
+  }
+  const float t = s0 + s1;
+  const float z = t - s0;
+  const float e = (s0 - (t - z)) + (s1 - z);
+  return t + ((c0 + c1) + e);
+}
+
 // bf16 storage of low parts: two values per 32-bit word, round to nearest
 // even (hardware conversion).
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -254,8 +254,7 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
         const float* M = s.mu + hb * m * (int64_t)m;
         float cm = -INFINITY;
         for (int b = lane; b < m_eff; b += 32) {
-          float u = 0.f;
-          for (int a = 0; a < m_eff; ++a) u = fmaf(hfh[a], M[a * m + b], u);
+          float u = dot2(hfh, M + b, m, m_eff);
           if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
           hgs[b] = u;
           cm = fmaxf(cm, f + hms[b]);

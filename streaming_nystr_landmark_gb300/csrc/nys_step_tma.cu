@@ -171,7 +171,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile 
 }
 
 // -------------------------------------------------------------- kernel
-template <int HT>
+template <int HT, int KD>
 __global__ void __launch_bounds__(kThreadsTma, 2)
 step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __restrict__ q,
                 const float* __restrict__ k, const float* __restrict__ v,
@@ -390,6 +390,19 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     for (int hh = 0; hh < HT; ++hh)
       qr[hh] = ck ? ld4(xq + hh * d + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 kev4 = ck ? ld4(xkev + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // d = 128 path: this lane's four float4 columns (kgl, kgl+8, kgl+16, kgl+24)
+    // of every head's query and of the evicted key.
+    const int kgrp = lane >> 3, kgl = lane & 7;
+    float4 qk[KD == 128 ? HT : 1][4];
+    float4 kvr[4];
+    if constexpr (KD == 128) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kvr[i] = ld4(xkev + 4 * (kgl + 8 * i));
+#pragma unroll
+        for (int hh = 0; hh < HT; ++hh) qk[hh][i] = ld4(xq + hh * 128 + 4 * (kgl + 8 * i));
+      }
+    }
 
     // ---- A: the K-side stages (sinks, window, key landmarks, Q~).
     for (int st = 0; st < P.n_k; ++st, advance()) {
@@ -397,6 +410,57 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       const float* stage = reinterpret_cast<const float*>(stage_ptr(ci));
       const int r0 = st * P.rows_k;
       const int nrow = min(P.rows_k, P.tot_k - r0);
+      if constexpr (KD == 128) {
+        // d = 128: a row is 32 float4; 8 lanes share a row (4 float4 each,
+        // query chunks in registers), a warp takes 4 rows at once.
+        for (int base = 0; base < nrow; base += kCWarps * 4) {
+          const int lr = base + warp * 4 + kgrp;
+          float x[HT];
+#pragma unroll
+          for (int hh = 0; hh < HT; ++hh) x[hh] = 0.f;
+          const bool valid = lr < nrow;
+          const int vr = r0 + lr;
+          if (valid) {
+            const float* row = stage + (size_t)lr * 128;
+            if (vr - ns == slot && vr >= ns) row = xknew;
+            const float4 a0 = ld4(row + 4 * kgl), a1 = ld4(row + 4 * (kgl + 8));
+            const float4 a2 = ld4(row + 4 * (kgl + 16)), a3 = ld4(row + 4 * (kgl + 24));
+            if (vr < ns + w + m) {
+#pragma unroll
+              for (int hh = 0; hh < HT; ++hh)
+                x[hh] = (dot4(a0, qk[hh][0]) + dot4(a1, qk[hh][1])) +
+                        (dot4(a2, qk[hh][2]) + dot4(a3, qk[hh][3]));
+            } else {
+              x[0] = (dot4(a0, kvr[0]) + dot4(a1, kvr[1])) + (dot4(a2, kvr[2]) + dot4(a3, kvr[3]));
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < HT; ++hh) {
+            x[hh] += __shfl_xor_sync(0xffffffffu, x[hh], 1);
+            x[hh] += __shfl_xor_sync(0xffffffffu, x[hh], 2);
+            x[hh] += __shfl_xor_sync(0xffffffffu, x[hh], 4);
+          }
+          if (valid && kgl == 0) {
+            if (vr < ns + w) {
+#pragma unroll
+              for (int hh = 0; hh < HT; ++hh)
+                if (hh < H) sig[hh * P.nrp + vr] = x[hh] * scale;
+            } else if (vr < ns + w + m) {
+#pragma unroll
+              for (int hh = 0; hh < HT; ++hh)
+                if (hh < H) fh[hh * P.mp + (vr - ns - w)] = x[hh] * scale;
+            } else {
+              int qr = vr - ns - w - m;
+              int h = 0;
+              while (qr >= m) {
+                qr -= m;
+                ++h;
+              }
+              lg[h * P.mp + qr] = x[0] * scale;
+            }
+          }
+        }
+      } else {
       for (int base = 0; base < nrow; base += kCWarps * kRowsPerRound) {
         float x[kRowsPerRound * HT];
 #pragma unroll
@@ -442,6 +506,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             }
           }
         }
+      }
       }
       release_slot(ci);
     }
@@ -509,8 +574,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         const float* Mh = reinterpret_cast<const float*>(stage_ptr(mslot)) + (size_t)mrow0 * m;
         float cm = -INFINITY;
         for (int b = lane; b < m_eff; b += 32) {
-          float u = 0.f;
-          for (int a = 0; a < m_eff; ++a) u = fmaf(hfh[a], Mh[a * m + b], u);
+          float u = dot2(hfh, Mh + b, m, m_eff);
           if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
           hgs[b] = u;
           cm = fmaxf(cm, f + hms[b]);
@@ -681,14 +745,27 @@ cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       sms = 1;
   }
-  cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)P.smem_bytes);
-  if (e != cudaSuccess) return e;
   const int64_t slots = (int64_t)sms * P.ctas_per_sm;
   const int64_t grid = n < slots ? n : slots;
-  step_tma_kernel<HT><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(s, P, g0, n, q, k,
-                                                                          v, out);
+  if constexpr (HT <= 2) {
+    if (s.d == 128) {
+      cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT, 128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)P.smem_bytes);
+      if (e != cudaSuccess) return e;
+      step_tma_kernel<HT, 128><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
+          s, P, g0, n, q, k, v, out);
+      return cudaGetLastError();
+    }
+  }
+  {
+    cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT, 0>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)P.smem_bytes);
+    if (e != cudaSuccess) return e;
+    step_tma_kernel<HT, 0><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
+        s, P, g0, n, q, k, v, out);
+  }
   return cudaGetLastError();
 }
 

@@ -31,6 +31,8 @@ def _run(wl, sample, dev, steps=None, check_every=None, n_groups=None,
         run.check_counters_all()
         run.check_state()
         assert run.flagged <= max(2, 0.01 * run.checked), (run.flagged, run.checked)
+        print(f"[parity] {wl.name}: {run.checked} rows, worst row error "
+              f"{run.worst:.2e}, flagged {run.flagged}")
         return run
     finally:
         run.close()
