@@ -319,21 +319,22 @@ def run_ours(args, wl):
         hk[i].normal_()
         hv[i].normal_()
     hout = torch.empty((G, H, wl.dv), pin_memory=True)
-    dq = torch.empty((G, H, wl.d), device=dev)
-    dk = torch.empty((G, wl.d), device=dev)
-    dvv = torch.empty((G, wl.dv), device=dev)
+    pipe = st.host_pipeline()
     e2e_steps = args.steps
     for i in range(2):
-        st.step_host(hq[i], hk[i], hv[i], hout, dq, dk, dvv, out)
-    torch.cuda.synchronize(dev)
+        pipe.submit(hq[i], hk[i], hv[i], hout)
+    pipe.synchronize()
     barrier(world)
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
     e2.record()
+    pipe.copy.wait_event(e2)  # the first token's input copy starts the clock
     for i in range(e2e_steps):
-        st.step_host(hq[i % pe], hk[i % pe], hv[i % pe], hout, dq, dk, dvv, out)
-    e3.record()
-    torch.cuda.synchronize(dev)
+        pipe.submit(hq[i % pe], hk[i % pe], hv[i % pe], hout)
+    # The timed region ends when the last token's outputs are on the host.
+    pipe.down.wait_stream(torch.cuda.current_stream(dev))
+    e3.record(pipe.down)
+    pipe.synchronize()
     barrier(world)
     dt_e2e = max_over_ranks(e2.elapsed_time(e3) / 1e3, world, dev)
     e2e = {"value": aggregate_rate(world, G, e2e_steps, dt_e2e), "unit": UNIT,
@@ -382,6 +383,111 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_layers(args, wl):
+    """Decode as a model runs it: one handle per layer (batch x KV groups
+    each), one launch per layer per token -- 28 dependent launches instead of
+    one fused launch -- eagerly or replayed from a CUDA graph."""
+    import torch
+    from streaming_nystr_landmark_gb300.nys import NystromStates
+    from streaming_nystr_landmark_gb300.workloads import DeviceFill
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L, H = wl.layers, wl.heads_per_kv
+    per = wl.seqs * wl.kv_groups
+    lw = wl.with_(layers=1)
+    layers = []
+    fill = DeviceFill(lw, dev, seed=2000 + rank)
+    seal_ms = 0.0
+    for _ in range(L):
+        st = NystromStates(wl.m, wl.w, wl.sink, H, wl.d, wl.dv, per, wl.rect, dev)
+        q = torch.empty((per, H, wl.t, wl.d), device=dev)
+        k = torch.empty((per, wl.t, wl.d), device=dev)
+        v = torch.empty((per, wl.t, wl.dv), device=dev)
+        fill.prompt_into(q, k, v)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        st.seal(q, k, v)
+        b.record()
+        torch.cuda.synchronize(dev)
+        seal_ms += a.elapsed_time(b)
+        del q, k, v
+        layers.append(st)
+    torch.cuda.empty_cache()
+    T = 8  # distinct decode tokens in the pool (and in one graph)
+    tq = torch.empty((T, L, per, H, wl.d), device=dev)
+    tk = torch.empty((T, L, per, wl.d), device=dev)
+    tv = torch.empty((T, L, per, wl.dv), device=dev)
+    for i in range(T):
+        fill.tokens_into(tq[i], tk[i], tv[i])
+    out = torch.empty((L, per, H, wl.dv), device=dev)
+
+    def token(i):
+        for l, st in enumerate(layers):
+            st.step(tq[i, l], tk[i, l], tv[i, l], out[l])
+
+    for i in range(args.warmup):
+        token(i % T)
+    torch.cuda.synchronize(dev)
+    graph = None
+    if args.mode == "layers-graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(T):
+                token(i)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    reps = max(1, args.steps // T) if graph is not None else args.steps
+    steps = reps * T if graph is not None else args.steps
+    barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    if graph is not None:
+        for _ in range(reps):
+            graph.replay()
+    else:
+        for i in range(steps):
+            token(i % T)
+    e1.record()
+    host_s = time.perf_counter() - t0
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    dt = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    for st in layers:
+        st.close()
+    if rank != 0:
+        return
+    G = L * per
+    peak, _ = measured_peak()
+    launch_s = dt / steps
+    achieved = algorithmic_bytes(wl) * G / launch_s / 1e9
+    line = {
+        "metric": METRIC, "value": aggregate_rate(world, G, steps, dt), "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * launch_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl, {
+            "mode": args.mode, "launches_per_token": L,
+            "groups_per_launch": per, "seal_ms_all_layers": seal_ms,
+            "host_enqueue_ms_per_token": 1e3 * host_s / steps,
+            "decode_input_pool": T}),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None},
+        "gpu_launches": steps * L,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,6 +500,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-groups", type=int, default=3)
+    ap.add_argument("--mode", choices=("fused", "layers", "layers-graph"),
+                    default="fused",
+                    help="fused: one launch per token over every layer's groups; "
+                         "layers: one launch per layer per token; layers-graph: "
+                         "the same launches replayed from a CUDA graph")
     ap.add_argument("--groups", type=int, default=0,
                     help="override the workload's group count (profiling on a "
                          "smaller case); 0 keeps the workload's own")
@@ -407,6 +518,8 @@ def main():
                       kv_groups=args.groups)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.mode != "fused":
+        run_layers(args, wl)
     else:
         run_ours(args, wl)
 

@@ -11,6 +11,19 @@
 
 namespace nys {
 
+// Raise a kernel's dynamic shared-memory limit only when a launch needs more
+// than any earlier one (one driver call per kernel and size, none during
+// later launches -- e.g. inside CUDA graph capture after a warm-up launch).
+template <auto Kernel>
+inline cudaError_t ensure_smem(size_t bytes) {
+  static size_t set_bytes = 48 * 1024;  // one record per kernel
+  if (bytes <= set_bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) set_bytes = bytes;
+  return e;
+}
+
 // Limits the kernels are written for (the ABI reports NYS_E_UNSUPPORTED
 // beyond them).  They bound the on-chip buffers: the seal keeps A, A^T A and
 // its Cholesky factor (3 m^2 doubles) in shared memory, and the step keeps a

@@ -496,19 +496,12 @@ template <int TR>
 cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, int t, int m_eff,
                           const float* k, const float* v, cudaStream_t stream) {
   const size_t bytes = replay_smem_floats(16 * TR, s.d) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(replay_kernel<TR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = ensure_smem<replay_kernel<TR>>(bytes);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
   replay_kernel<TR><<<dim3((unsigned)(n * s.heads), tiles), kThreads, bytes, stream>>>(
       s, g0, t, m_eff, k, v);
   return cudaGetLastError();
-}
-
-cudaError_t set_smem(const void* fn, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)bytes);
 }
 
 }  // namespace
@@ -527,7 +520,7 @@ cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const size_t pbytes = pinv_smem_doubles(m_eff) * sizeof(double);
-  if ((e = set_smem((const void*)pinv_kernel, pbytes)) != cudaSuccess) return e;
+  if ((e = ensure_smem<pinv_kernel>(pbytes)) != cudaSuccess) return e;
   pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, m_eff, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

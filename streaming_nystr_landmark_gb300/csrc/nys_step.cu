@@ -382,11 +382,8 @@ cudaError_t launch_tile(const DevState& s, int64_t g0, int64_t n,
                         float* out, cudaStream_t stream) {
   const StepSmem L(HT, s.d, s.dv, s.sink + s.w, s.m);
   const size_t bytes = (size_t)L.total * sizeof(float);
-  if (bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        step_kernel<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = ensure_smem<step_kernel<HT>>(bytes);
+  if (e != cudaSuccess) return e;
   step_kernel<HT><<<(unsigned)n, kThreads, bytes, stream>>>(s, g0, q, k, v, out);
   return cudaGetLastError();
 }

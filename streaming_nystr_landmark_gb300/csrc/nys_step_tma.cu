@@ -749,9 +749,7 @@ cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64
   const int64_t grid = n < slots ? n : slots;
   if constexpr (HT <= 2) {
     if (s.d == 128) {
-      cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT, 128>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)P.smem_bytes);
+      cudaError_t e = ensure_smem<step_tma_kernel<HT, 128>>(P.smem_bytes);
       if (e != cudaSuccess) return e;
       step_tma_kernel<HT, 128><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
           s, P, g0, n, q, k, v, out);
@@ -759,9 +757,7 @@ cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64
     }
   }
   {
-    cudaError_t e = cudaFuncSetAttribute(step_tma_kernel<HT, 0>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)P.smem_bytes);
+    cudaError_t e = ensure_smem<step_tma_kernel<HT, 0>>(P.smem_bytes);
     if (e != cudaSuccess) return e;
     step_tma_kernel<HT, 0><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
         s, P, g0, n, q, k, v, out);

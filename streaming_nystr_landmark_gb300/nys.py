@@ -248,6 +248,10 @@ class NystromStates:
         hout.copy_(dout, non_blocking=True)
         return hout
 
+    def host_pipeline(self, n=None, depth=2):
+        """A pipelined host-buffer driver for this handle (see HostPipeline)."""
+        return HostPipeline(self, self.n_groups if n is None else n, depth)
+
     def query(self, g):
         return nys_query(self.handle, g, self.cfg.heads_per_kv, self._stream())
 
@@ -291,3 +295,60 @@ class NystromStates:
 
     def mark_sealed(self, g0=0, n=None):
         nys_mark_sealed(self.handle, g0, self.n_groups if n is None else n)
+
+
+class HostPipeline:
+    """Decode tokens from pinned host buffers with copies overlapped.
+
+    Each ``submit`` enqueues, for one token: the host->device copy of q, k, v
+    on an upload stream into one of ``depth`` device staging slots, the
+    decode launch on the compute stream once that copy has landed, and the
+    device->host copy of the outputs on a separate download stream once the
+    launch is done.  Token n+1's inputs therefore travel while token n
+    computes (uploads never queue behind downloads), and a staging slot is
+    reused only after the launch that read it has finished.
+    ``synchronize`` waits for everything submitted.  All ordering is by CUDA
+    events; the decode itself is nys_step_batch.
+    """
+
+    def __init__(self, states, n, depth=2):
+        import torch
+        self.torch = torch
+        self.st = states
+        self.n = n
+        c = states.cfg
+        dev = states.device
+        self.compute = torch.cuda.current_stream(dev)
+        self.copy = torch.cuda.Stream(dev)      # uploads
+        self.down = torch.cuda.Stream(dev)      # downloads
+        mk = lambda *shape: torch.empty(shape, device=dev)
+        self.slots = [dict(q=mk(n, c.heads_per_kv, c.d), k=mk(n, c.d), v=mk(n, c.dv),
+                           out=mk(n, c.heads_per_kv, c.dv),
+                           loaded=torch.cuda.Event(), done=torch.cuda.Event(),
+                           drained=torch.cuda.Event())
+                      for _ in range(depth)]
+        for sl in self.slots:
+            sl["done"].record(self.compute)
+            sl["drained"].record(self.down)
+        self.i = 0
+
+    def submit(self, hq, hk, hv, hout):
+        sl = self.slots[self.i % len(self.slots)]
+        self.i += 1
+        with self.torch.cuda.stream(self.copy):
+            self.copy.wait_event(sl["done"])       # the last launch read this slot
+            sl["q"].copy_(hq, non_blocking=True)
+            sl["k"].copy_(hk, non_blocking=True)
+            sl["v"].copy_(hv, non_blocking=True)
+            sl["loaded"].record(self.copy)
+        self.compute.wait_event(sl["loaded"])
+        self.compute.wait_event(sl["drained"])      # its previous outputs left
+        self.st.step(sl["q"], sl["k"], sl["v"], sl["out"])
+        sl["done"].record(self.compute)
+        with self.torch.cuda.stream(self.down):
+            self.down.wait_event(sl["done"])
+            hout.copy_(sl["out"], non_blocking=True)
+            sl["drained"].record(self.down)
+
+    def synchronize(self):
+        self.torch.cuda.synchronize(self.st.device)

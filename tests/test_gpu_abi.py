@@ -160,3 +160,93 @@ def test_step_kernel_on_uploaded_oracle_state(cuda_device):
             for h in range(3):
                 assert row_err(got[g, h], ref[h]) <= OUT_TOL, (n, g, h)
     st.close()
+
+
+def test_host_pipeline_matches_direct_steps(cuda_device):
+    """The pipelined host path (copies on a side stream, double-buffered
+    device staging) yields exactly the outputs of plain launches on device
+    inputs, token after token."""
+    import torch
+    wl, st_a = _small(cuda_device, groups=5)
+    _, st_b = _small(cuda_device, groups=5)
+    q, k, v, gens = host_prompt_batch(wl, range(5))
+    qd, kd, vd = _to(cuda_device, q, k, v)
+    st_a.seal(qd, kd, vd)
+    st_b.seal(qd, kd, vd)
+    pipe = st_b.host_pipeline()
+    outs_host = []
+    outs_dev = []
+    for n in range(12):
+        tq, tk, tv = host_token_batch(gens, n)
+        hq, hk, hv = [torch.from_numpy(a).pin_memory() for a in (tq, tk, tv)]
+        hout = torch.empty((5, 2, 32), pin_memory=True)
+        pipe.submit(hq, hk, hv, hout)
+        outs_host.append(hout)
+        out = torch.empty((5, 2, 32), device=cuda_device)
+        st_a.step(*_to(cuda_device, tq, tk, tv), out)
+        outs_dev.append(out)
+    pipe.synchronize()
+    for a, b in zip(outs_dev, outs_host):
+        assert torch.equal(a.cpu(), b)
+    st_a.close()
+    st_b.close()
+
+
+def test_per_layer_launches_and_graph_replay_match_fused(cuda_device):
+    """A model steps one layer at a time: per-layer handles stepped with one
+    launch each, eagerly or replayed from a CUDA graph, give bit-identical
+    outputs and state to one fused launch over all layers' groups."""
+    import torch
+    L, per = 3, 6
+    wl = Workload("layers", 2, 32, 32, 8, 16, 4, 0, 64, 8, 1, 1, L * per, "unit2", seed=9)
+    q, k, v, gens = host_prompt_batch(wl, range(L * per))
+    mk = lambda n: nys.NystromStates(wl.m, wl.w, wl.sink, 2, 32, 32, n, 0, cuda_device)
+    fused = mk(L * per)
+    fused.seal(*_to(cuda_device, q, k, v))
+    eager = [mk(per) for _ in range(L)]
+    graphed = [mk(per) for _ in range(L)]
+    for l in range(L):
+        sl = slice(l * per, (l + 1) * per)
+        for st in (eager[l], graphed[l]):
+            st.seal(*_to(cuda_device, q[sl], k[sl], v[sl]))
+    tq = torch.empty((L * per, 2, 32), device=cuda_device)
+    tk = torch.empty((L * per, 32), device=cuda_device)
+    tv = torch.empty((L * per, 32), device=cuda_device)
+    out_f = torch.empty((L * per, 2, 32), device=cuda_device)
+    out_e = torch.empty_like(out_f)
+    out_g = torch.empty_like(out_f)
+
+    def layered(states, out):
+        for l, st in enumerate(states):
+            sl = slice(l * per, (l + 1) * per)
+            st.step(tq[sl], tk[sl], tv[sl], out[sl])
+
+    # warm up the graphed handles once, outside capture, on token 0
+    th = host_token_batch(gens, 0)
+    for dst, src in zip((tq, tk, tv), th):
+        dst.copy_(torch.from_numpy(src))
+    fused.step(tq, tk, tv, out_f)
+    layered(eager, out_e)
+    layered(graphed, out_g)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f, out_e) and torch.equal(out_f, out_g)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layered(graphed, out_g)
+    for n in range(1, 8):
+        th = host_token_batch(gens, n)
+        for dst, src in zip((tq, tk, tv), th):
+            dst.copy_(torch.from_numpy(src))
+        fused.step(tq, tk, tv, out_f)
+        layered(eager, out_e)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_f, out_e), n
+        assert torch.equal(out_f, out_g), n
+    for name in ("t_hat", "t_lo", "z_hat", "m_max", "far_len", "ints", "win_k"):
+        whole = fused.region(name)
+        for l in range(L):
+            assert torch.equal(whole[l * per:(l + 1) * per], eager[l].region(name)), name
+            assert torch.equal(whole[l * per:(l + 1) * per], graphed[l].region(name)), name
+    for st in [fused] + eager + graphed:
+        st.close()
