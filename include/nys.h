@@ -181,6 +181,23 @@ int nys_free_states(nys_states* st);
 int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t,
              const float* q, const float* k, const float* v, void* stream);
 
+/* nys_seal for a batch of prompts of different lengths, in one set of
+ * launches (nystrom.rs, NystromState::prefill_group applied to each group
+ * with its own t; prefill_shared fixes m_eff = clamp(t/8, 4, m) per group,
+ * so the effective landmark count may differ between groups of the batch).
+ * t_host: host array of n prompt lengths, each > w + sink + 8.
+ * Inputs are packed back to back in group order: with off_i = t_0 + ... +
+ * t_{i-1}, group g0+i's keys are rows off_i .. off_i + t_i - 1 of
+ * k [sum t][d], its values the same rows of v [sum t][dv], and its queries
+ * the H*t_i rows starting at row H*off_i of q [H * sum t][d], laid out
+ * [H][t_i][d] (all device).  Allocates the f64 workspace and an n*16-byte
+ * table of per-group lengths, landmark counts and offsets with
+ * cudaMallocAsync on `stream`, and frees both there.
+ * Errors: those of nys_seal; NYS_E_EXACT_ONLY or NYS_E_RANGE if any t_i is
+ * outside the landmark path (nothing is launched then). */
+int nys_seal_ragged(nys_states* st, int64_t g0, int64_t n, const int32_t* t_host,
+                    const float* q, const float* k, const float* v, void* stream);
+
 /* One decode token for groups [g0, g0+n) (nystrom.rs,
  * NystromState::step_group and advance, NystromHead::step and far_insert;
  * Struct NystromState, step_group): insert each group's (k, v) once -- a full

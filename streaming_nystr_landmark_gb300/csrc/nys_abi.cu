@@ -274,6 +274,76 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
   return NYS_OK;
 }
 
+int nys_seal_ragged(nys_states* st, int64_t g0, int64_t n, const int32_t* t_host,
+                    const float* q, const float* k, const float* v, void* stream) {
+  if (!st) return NYS_E_INVAL;
+  int rc = check_range(st, g0, n);
+  if (rc) return rc;
+  if (n == 0) return NYS_OK;
+  if (!t_host || !q || !k || !v) return NYS_E_INVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
+  const nys_config& c = st->cfg;
+  // Per-group geometry, packed for one upload: t, m_eff (int32 each), then
+  // the first row of every group's prompt (int64).
+  std::vector<int32_t> ti((size_t)n), mi((size_t)n);
+  std::vector<int64_t> off((size_t)n);
+  int64_t rows = 0;
+  int max_me = 0, min_me = c.m, clamp_t = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t t = t_host[i];
+    if (t < 1) return NYS_E_RANGE;
+    if ((int64_t)t <= (int64_t)c.w + c.sink + 8) return NYS_E_EXACT_ONLY;
+    const int me = std::min(std::max(t / 8, 4), c.m);
+    ti[(size_t)i] = t;
+    mi[(size_t)i] = me;
+    off[(size_t)i] = rows;
+    rows += t;
+    max_me = std::max(max_me, me);
+    if (me < min_me) {
+      min_me = me;
+      clamp_t = t;
+    }
+  }
+  if (min_me < c.m && !g_clamp_said.exchange(true)) {
+    std::fprintf(stderr,
+                 "nys: landmark budget m=%d clamped to m_eff=%d: the prompt is %d tokens and "
+                 "the landmarks take t/8; seal at least %d tokens to use the whole budget\n",
+                 c.m, min_me, clamp_t, c.m * 8);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const nys::DevState ds = dev_state(st);
+  const size_t per = nys::seal_workspace_bytes_per_group(ds);
+  int64_t chunk = (int64_t)(kWorkspaceBudget / per);
+  if (chunk < 1) chunk = 1;
+  if (chunk > n) chunk = n;
+  const size_t meta_bytes = (size_t)n * 16;
+  void* ws = nullptr;
+  void* meta = nullptr;
+  if (cudaMallocAsync(&ws, per * (size_t)chunk, s) != cudaSuccess) return NYS_E_CUDA;
+  if (cudaMallocAsync(&meta, meta_bytes, s) != cudaSuccess) {
+    cudaFreeAsync(ws, s);
+    return NYS_E_CUDA;
+  }
+  int64_t* off_dev = static_cast<int64_t*>(meta);
+  int32_t* t_dev = reinterpret_cast<int32_t*>(off_dev + n);
+  int32_t* me_dev = t_dev + n;
+  cudaError_t e = cudaMemcpyAsync(off_dev, off.data(), (size_t)n * 8, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(t_dev, ti.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(me_dev, mi.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s);
+  for (int64_t a = 0; a < n && e == cudaSuccess; a += chunk) {
+    const int64_t nb = std::min(chunk, n - a);
+    const nys::SealGeom sg{0, 0, t_dev + a, me_dev + a, off_dev + a};
+    e = nys::launch_seal_geom(ds, g0 + a, nb, sg, max_me, q, k, v, static_cast<double*>(ws), s);
+  }
+  const cudaError_t f1 = cudaFreeAsync(ws, s), f2 = cudaFreeAsync(meta, s);
+  // The host arrays above were staged by the copies before they returned.
+  if (e != cudaSuccess || f1 != cudaSuccess || f2 != cudaSuccess) return NYS_E_CUDA;
+  std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  return NYS_OK;
+}
+
 int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
                    const float* k, const float* v, float* out, void* stream) {
   if (!st) return NYS_E_INVAL;

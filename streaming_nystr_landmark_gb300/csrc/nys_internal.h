@@ -159,6 +159,31 @@ cudaError_t launch_step_tma(const DevState& s, const void* plan, int64_t g0, int
                             const float* q, const float* k, const float* v, float* out,
                             cudaStream_t stream);
 
+// Prompt geometry of a seal launch.  Uniform batches (every group has prompt
+// length t and m_eff landmarks, group i's rows start at i * t) leave the
+// arrays null; ragged batches give per-group length, landmark count and
+// first row (device arrays indexed by the group's position in the launch).
+struct SealGeom {
+  int t, m_eff;
+  const int32_t* t_arr;
+  const int32_t* me_arr;
+  const int64_t* off_arr;
+};
+#ifdef __CUDACC__
+__device__ __forceinline__ void seal_geom(const SealGeom& sg, int64_t gi, int& t, int& me,
+                                          int64_t& off) {
+  if (sg.t_arr) {
+    t = sg.t_arr[gi];
+    me = sg.me_arr[gi];
+    off = sg.off_arr[gi];
+  } else {
+    t = sg.t;
+    me = sg.m_eff;
+    off = gi * (int64_t)sg.t;
+  }
+}
+#endif
+
 // Bytes of f64 workspace the seal needs per group (key landmarks and every
 // head's query landmarks before rounding).
 size_t seal_workspace_bytes_per_group(const DevState& s);
@@ -169,6 +194,13 @@ size_t seal_workspace_bytes_per_group(const DevState& s);
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
                         const float* v, double* ws, cudaStream_t stream);
+
+// Seal with per-group prompt geometry (sg's arrays on the device, indexed
+// from 0 for group g0); max_me bounds every group's m_eff.  q, k, v point at
+// the start of the packed batch.
+cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
+                             int max_me, const float* q, const float* k, const float* v,
+                             double* ws, cudaStream_t stream);
 
 // Host-side checks of a seal request, identical to nys_seal's, for entry
 // points that supply their own workspace.  Fills the device view and m_eff

@@ -45,7 +45,7 @@ __device__ __forceinline__ void st4(float* p, float4 x) {
 
 // ---------------------------------------------------------------- 1
 __global__ void __launch_bounds__(kThreads)
-landmarks_kernel(DevState s, int64_t g0, int t, int m_eff,
+landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
                  const float* __restrict__ q, const float* __restrict__ k,
                  const float* __restrict__ v, double* __restrict__ ws) {
   __shared__ double red[kWarps][128];
@@ -54,14 +54,17 @@ landmarks_kernel(DevState s, int64_t g0, int t, int m_eff,
   const int r = blockIdx.y;  // 0: keys, 1 + h: queries of head h
   const int d = s.d, dv = s.dv, H = s.heads, m = s.m, w = s.w, ns = s.sink;
   const int d4 = d >> 2, dv4 = dv >> 2;
+  int t, m_eff;
+  int64_t off;
+  seal_geom(sg, gi, t, m_eff, off);
 
   const float* src;
   float* dst32;
   if (r == 0) {
-    src = k + gi * (int64_t)t * d;
+    src = k + off * d;
     dst32 = s.k_tilde + g * m * (int64_t)d;
   } else {
-    src = q + ((gi * H + (r - 1)) * (int64_t)t) * d;
+    src = q + (off * H + (int64_t)(r - 1) * t) * d;
     dst32 = s.q_tilde + ((g * H + (r - 1)) * m) * (int64_t)d;
   }
   double* dst64 = ws + (gi * (1 + H) + r) * (int64_t)m * d;
@@ -103,7 +106,7 @@ landmarks_kernel(DevState s, int64_t g0, int t, int m_eff,
 
   if (r != 0) return;
   // Sinks: positions 0..sink, permanent (prefill_shared).
-  const float* vsrc = v + gi * (int64_t)t * dv;
+  const float* vsrc = v + off * dv;
   for (int idx = tid; idx < ns * d4; idx += kThreads)
     st4(s.sink_k + g * ns * (int64_t)d + 4 * idx, ld4(src + 4 * idx));
   for (int idx = tid; idx < ns * dv4; idx += kThreads)
@@ -144,14 +147,17 @@ __host__ __device__ inline size_t pinv_smem_doubles(int me) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-pinv_kernel(DevState s, int64_t g0, int m_eff, const double* __restrict__ ws) {
+pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) {
   extern __shared__ __align__(16) double dsm[];
   __shared__ int fail;
   __shared__ double lam_s, mean_diag_s;
   const int tid = threadIdx.x;
-  const int H = s.heads, m = s.m, d = s.d, me = m_eff;
+  const int H = s.heads, m = s.m, d = s.d;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
   const int h = (int)(blockIdx.x - gi * H);
+  int t_unused, me;
+  int64_t off_unused;
+  seal_geom(sg, gi, t_unused, me, off_unused);
   double* A = dsm;            // [me][me]
   double* G = A + me * me;    // [me][me]  A^T A
   double* Lf = G + me * me;   // [me][me]  Cholesky factor / working copy
@@ -315,16 +321,19 @@ __device__ __forceinline__ void load_rows(const float* p, float (&a)[TR]) {
 
 template <int TR>
 __global__ void __launch_bounds__(kThreads, 2)
-replay_kernel(DevState s, int64_t g0, int t, int m_eff,
+replay_kernel(DevState s, int64_t g0, SealGeom sg,
               const float* __restrict__ k, const float* __restrict__ v) {
   constexpr int RT = 16 * TR;
   extern __shared__ __align__(16) float fsm[];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int H = s.heads, m = s.m, d = s.d, dv = s.dv, w = s.w, ns = s.sink;
-  const int d4 = d >> 2, me = m_eff;
+  const int d4 = d >> 2;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
   const int h = (int)(blockIdx.x - gi * H);
   const int64_t hb = g * H + h;
+  int t, me;
+  int64_t off;
+  seal_geom(sg, gi, t, me, off);
   const int c0 = blockIdx.y * kValTile;
   const int cw = min(kValTile, dv - c0);
   const float scale = s.scale;
@@ -352,8 +361,8 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
     }
   }
 
-  const float* ksrc = k + gi * (int64_t)t * d;
-  const float* vsrc = v + gi * (int64_t)t * dv + c0;
+  const float* ksrc = k + off * d;
+  const float* vsrc = v + off * dv + c0;
   const int j_end = t - w;  // keys sink .. t-w-1 were evicted by the replay
   const int klane = tid & 15, kchunk = tid >> 4;  // 16 keys x 16 chunk lanes
   for (int j0 = ns; j0 < j_end; j0 += kKeyBlock) {
@@ -493,14 +502,14 @@ replay_kernel(DevState s, int64_t g0, int t, int m_eff,
 }
 
 template <int TR>
-cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, int t, int m_eff,
+cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
                           const float* k, const float* v, cudaStream_t stream) {
   const size_t bytes = replay_smem_floats(16 * TR, s.d) * sizeof(float);
   cudaError_t e = ensure_smem<replay_kernel<TR>>(bytes);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
   replay_kernel<TR><<<dim3((unsigned)(n * s.heads), tiles), kThreads, bytes, stream>>>(
-      s, g0, t, m_eff, k, v);
+      s, g0, sg, k, v);
   return cudaGetLastError();
 }
 
@@ -510,23 +519,30 @@ size_t seal_workspace_bytes_per_group(const DevState& s) {
   return (size_t)(1 + s.heads) * s.m * s.d * sizeof(double);
 }
 
+cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
+                             int max_me, const float* q, const float* k, const float* v,
+                             double* ws, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  cudaError_t e;
+  landmarks_kernel<<<dim3((unsigned)n, 1 + s.heads), kThreads, 0, stream>>>(s, g0, sg, q, k, v,
+                                                                            ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const size_t pbytes = pinv_smem_doubles(max_me) * sizeof(double);
+  if ((e = ensure_smem<pinv_kernel>(pbytes)) != cudaSuccess) return e;
+  pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, sg, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  if (max_me <= 16) return launch_replay<1>(s, g0, n, sg, k, v, stream);
+  if (max_me <= 32) return launch_replay<2>(s, g0, n, sg, k, v, stream);
+  return launch_replay<4>(s, g0, n, sg, k, v, stream);
+}
+
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
                         const float* v, double* ws, cudaStream_t stream) {
-  if (n <= 0) return cudaSuccess;
-  cudaError_t e;
-  landmarks_kernel<<<dim3((unsigned)n, 1 + s.heads), kThreads, 0, stream>>>(
-      s, g0, t, m_eff, q, k, v, ws);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  const size_t pbytes = pinv_smem_doubles(m_eff) * sizeof(double);
-  if ((e = ensure_smem<pinv_kernel>(pbytes)) != cudaSuccess) return e;
-  pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, m_eff, ws);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  if (m_eff <= 16) return launch_replay<1>(s, g0, n, t, m_eff, k, v, stream);
-  if (m_eff <= 32) return launch_replay<2>(s, g0, n, t, m_eff, k, v, stream);
-  return launch_replay<4>(s, g0, n, t, m_eff, k, v, stream);
+  const SealGeom sg{t, m_eff, nullptr, nullptr, nullptr};
+  return launch_seal_geom(s, g0, n, sg, m_eff, q, k, v, ws, stream);
 }
 
 }  // namespace nys

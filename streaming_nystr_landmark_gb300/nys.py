@@ -32,7 +32,7 @@ NYS_RECT_FM = 1
 EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
             "nys_seal", "nys_step_batch", "nys_query", "nys_layout_of",
             "nys_mark_sealed", "nys_config_of", "nys_strerror",
-            "nys_seal_static")
+            "nys_seal_static", "nys_seal_ragged")
 
 
 class NysConfig(ctypes.Structure):
@@ -79,6 +79,7 @@ def _load():
         "nys_config_of": [VP, P(NysConfig), P(I64)],
         "nys_strerror": [ctypes.c_int],
         "nys_seal_static": [VP, I64, I64, I32, VP, VP, VP, VP],
+        "nys_seal_ragged": [VP, I64, I64, P(I32), VP, VP, VP, VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -137,6 +138,15 @@ def nys_seal_static(handle, g0, n, t, q, k, v, stream=0):
     (for callers that cannot allocate device memory while they run)."""
     _check(_lib.nys_seal_static(handle, g0, n, t, q, k, v, stream or None),
            "nys_seal_static")
+
+
+def nys_seal_ragged(handle, g0, t_list, q, k, v, stream=0):
+    """Seal len(t_list) groups from g0 on prompts of the given lengths,
+    packed back to back (see include/nys.h)."""
+    n = len(t_list)
+    arr = (ctypes.c_int32 * max(n, 1))(*t_list)
+    _check(_lib.nys_seal_ragged(handle, g0, n, arr, q, k, v, stream or None),
+           "nys_seal_ragged")
 
 
 def nys_step_batch(handle, g0, n, q, k, v, out, stream=0):
@@ -224,6 +234,17 @@ class NystromStates:
                  _ptr(q, torch.float32, (n, c.heads_per_kv, t, c.d), "q"),
                  _ptr(k, torch.float32, (n, t, c.d), "k"),
                  _ptr(v, torch.float32, (n, t, c.dv), "v"), self._stream())
+
+    def seal_ragged(self, t_list, q, k, v, g0=0):
+        """Seal groups g0.. on prompts of lengths t_list packed back to back:
+        k [sum t][d], v [sum t][dv], q [H * sum t][d] (per group [H][t][d])."""
+        c = self.cfg
+        torch = self.torch
+        total = int(sum(t_list))
+        nys_seal_ragged(self.handle, g0, list(t_list),
+                        _ptr(q, torch.float32, (c.heads_per_kv * total, c.d), "q"),
+                        _ptr(k, torch.float32, (total, c.d), "k"),
+                        _ptr(v, torch.float32, (total, c.dv), "v"), self._stream())
 
     def step(self, q, k, v, out, g0=0, n=None):
         c = self.cfg

@@ -90,43 +90,9 @@ class ParityRun:
     # ------------------------------------------------------------ state
     def check_state(self, far_tol=FAR_TOL):
         """Compare every sampled group's device state with its oracle."""
-        torch = self.torch
-        st = self.st
-        reg = {name: st.region(name).cpu().numpy() for name in (
-            "win_k", "win_v", "sink_k", "sink_v", "k_tilde", "q_tilde", "mu",
-            "m_max", "far_len", "ints")}
-        reg["t_hat"] = st.far_numerator()
-        reg["z_hat"] = st.far_denominator()
+        regs = read_state(self.st)
         for o, g in zip(self.oracles, self.sample):
-            me = o.m_eff
-            ints = reg["ints"][g]
-            assert ints[0] == o.win_head and ints[1] == o.win_len, (g, ints)
-            assert ints[2] == me and ints[4] == 1, (g, ints)
-            np.testing.assert_array_equal(reg["win_k"][g], o.win_k.astype(np.float32))
-            np.testing.assert_array_equal(reg["win_v"][g], o.win_v.astype(np.float32))
-            if o.sink_len:
-                np.testing.assert_array_equal(reg["sink_k"][g], o.sink_k.astype(np.float32))
-                np.testing.assert_array_equal(reg["sink_v"][g], o.sink_v.astype(np.float32))
-            kt = reg["k_tilde"][g][:me].astype(np.float64)
-            _close_rows(kt, o.k_tilde, LANDMARK_TOL, "k_tilde", g)
-            for h, hs in enumerate(o.hs):
-                assert reg["far_len"][g][h] == hs.far_len, (g, h)
-                _close_rows(reg["q_tilde"][g][h][:me].astype(np.float64),
-                            hs.q_tilde, LANDMARK_TOL, "q_tilde", g)
-                mu = reg["mu"][g][h][:me, :me].astype(np.float64)
-                rel = np.linalg.norm(mu - hs.mu) / np.linalg.norm(hs.mu)
-                assert rel <= MU_TOL, ("mu", g, h, rel)
-                mm = reg["m_max"][g][h][:me].astype(np.float64)
-                assert np.all(np.abs(mm - hs.m_max) <= far_tol * np.maximum(1.0, np.abs(hs.m_max))), \
-                    ("m_max", g, h, np.abs(mm - hs.m_max).max())
-                # Bring the device accumulators to the oracle's scale.
-                rescale = np.exp(mm - hs.m_max)
-                z = reg["z_hat"][g][h][:me].astype(np.float64) * rescale
-                np.testing.assert_allclose(z, hs.z_hat, rtol=far_tol, atol=0)
-                t = reg["t_hat"][g][h][:me].astype(np.float64) * rescale[:, None]
-                for b in range(me):
-                    e = row_err(t[b], hs.t_hat[b])
-                    assert e <= far_tol, ("t_hat", g, h, b, e)
+            compare_group_state(regs, g, o, far_tol)
 
     # ------------------------------------------------------------ decode
     def step(self):
@@ -179,6 +145,49 @@ class ParityRun:
 
     def close(self):
         self.st.close()
+
+
+def read_state(st):
+    """Host copies of every state region (T^ and Z^ as hi + lo)."""
+    reg = {name: st.region(name).cpu().numpy() for name in (
+        "win_k", "win_v", "sink_k", "sink_v", "k_tilde", "q_tilde", "mu",
+        "m_max", "far_len", "ints")}
+    reg["t_hat"] = st.far_numerator()
+    reg["z_hat"] = st.far_denominator()
+    return reg
+
+
+def compare_group_state(reg, g, o, far_tol=FAR_TOL):
+    """Device state of group g (from read_state) against oracle o."""
+    me = o.m_eff
+    ints = reg["ints"][g]
+    assert ints[0] == o.win_head and ints[1] == o.win_len, (g, ints)
+    assert ints[2] == me and ints[4] == 1, (g, ints)
+    np.testing.assert_array_equal(reg["win_k"][g], o.win_k.astype(np.float32))
+    np.testing.assert_array_equal(reg["win_v"][g], o.win_v.astype(np.float32))
+    if o.sink_len:
+        np.testing.assert_array_equal(reg["sink_k"][g], o.sink_k.astype(np.float32))
+        np.testing.assert_array_equal(reg["sink_v"][g], o.sink_v.astype(np.float32))
+    _close_rows(reg["k_tilde"][g][:me].astype(np.float64), o.k_tilde, LANDMARK_TOL,
+                "k_tilde", g)
+    for h, hs in enumerate(o.hs):
+        assert reg["far_len"][g][h] == hs.far_len, (g, h)
+        _close_rows(reg["q_tilde"][g][h][:me].astype(np.float64), hs.q_tilde,
+                    LANDMARK_TOL, "q_tilde", g)
+        mu = reg["mu"][g][h][:me, :me].astype(np.float64)
+        rel = np.linalg.norm(mu - hs.mu) / np.linalg.norm(hs.mu)
+        assert rel <= MU_TOL, ("mu", g, h, rel)
+        mm = reg["m_max"][g][h][:me].astype(np.float64)
+        assert np.all(np.abs(mm - hs.m_max) <= far_tol * np.maximum(1.0, np.abs(hs.m_max))), \
+            ("m_max", g, h, np.abs(mm - hs.m_max).max())
+        # Bring the device accumulators to the oracle's scale.
+        rescale = np.exp(mm - hs.m_max)
+        z = reg["z_hat"][g][h][:me].astype(np.float64) * rescale
+        np.testing.assert_allclose(z, hs.z_hat, rtol=far_tol, atol=0)
+        t = reg["t_hat"][g][h][:me].astype(np.float64) * rescale[:, None]
+        for b in range(me):
+            e = row_err(t[b], hs.t_hat[b])
+            assert e <= far_tol, ("t_hat", g, h, b, e)
 
 
 def _close_rows(got, ref, tol, what, g):
