@@ -488,6 +488,56 @@ def run_layers(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def run_seal(args, wl):
+    """Time the seal: one uniform batch at the workload's prompt length, and
+    one ragged batch of the same groups whose lengths are spread uniformly
+    over [t/2, 3t/2] (about the same number of prompt tokens)."""
+    import numpy as np
+    import torch
+    from streaming_nystr_landmark_gb300.nys import NystromStates
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    G, H = wl.n_groups, wl.heads_per_kv
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    rng = np.random.default_rng(77)
+    ts = rng.integers(wl.t // 2, 3 * wl.t // 2 + 1, size=G).astype(np.int32)
+    ts = np.maximum(ts, wl.w + wl.sink + 9)
+    res = {}
+    for kind, total in (("uniform", G * wl.t), ("ragged", int(ts.sum()))):
+        st = NystromStates(wl.m, wl.w, wl.sink, H, wl.d, wl.dv, G, wl.rect, dev)
+        q = torch.randn((H * total, wl.d), device=dev, generator=gen)
+        k = torch.randn((total, wl.d), device=dev, generator=gen)
+        v = torch.randn((total, wl.dv), device=dev, generator=gen)
+        times = []
+        for rep in range(args.warmup + 3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            if kind == "uniform":
+                st.seal(q.view(G, H, wl.t, wl.d), k.view(G, wl.t, wl.d),
+                        v.view(G, wl.t, wl.dv))
+            else:
+                st.seal_ragged(ts.tolist(), q, k, v)
+            b.record()
+            torch.cuda.synchronize(dev)
+            if rep >= args.warmup:
+                times.append(a.elapsed_time(b))
+        res[kind] = {"ms": min(times), "prompt_tokens": total,
+                     "tokens_per_s": total / (min(times) / 1e3)}
+        st.close()
+        del q, k, v
+        torch.cuda.empty_cache()
+    line = {"metric": "Nyström seal ms per batch (uniform vs ragged prompts)",
+            "value": res["ragged"]["ms"], "unit": "ms", "higher_is_better": False,
+            "n_gpus": 1, "steps": 3, "warmup": args.warmup, "dtype": "f32+f64",
+            "data": "synthetic",
+            "config": workload_config(wl, {"ragged_t_range": [int(ts.min()), int(ts.max())],
+                                           "uniform": res["uniform"],
+                                           "ragged": res["ragged"]})}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -500,7 +550,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-groups", type=int, default=3)
-    ap.add_argument("--mode", choices=("fused", "layers", "layers-graph"),
+    ap.add_argument("--mode", choices=("fused", "layers", "layers-graph", "seal"),
                     default="fused",
                     help="fused: one launch per token over every layer's groups; "
                          "layers: one launch per layer per token; layers-graph: "
@@ -518,6 +568,8 @@ def main():
                       kv_groups=args.groups)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.mode == "seal":
+        run_seal(args, wl)
     elif args.mode != "fused":
         run_layers(args, wl)
     else:
