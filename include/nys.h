@@ -54,8 +54,9 @@ typedef enum {
   NYS_E_CUDA = -7,       /* a CUDA call or kernel launch failed               */
   NYS_E_UNSUPPORTED = -8, /* geometry beyond the kernels' limits: m > 64,
                             d or dv > 256, heads_per_kv > 64, sink + w > 2048  */
-  NYS_E_SCRATCH = -9     /* nys_seal_static only: one group's workspace does
+  NYS_E_SCRATCH = -9,    /* nys_seal_static only: one group's workspace does
                             not fit the library's static scratch array         */
+  NYS_E_CAPACITY = -10   /* an exact-only group would exceed exact_cap keys   */
 } nys_status;
 
 /* Rectifier of the skeleton's far mass (nystrom.rs, enum O1Rect).
@@ -75,6 +76,8 @@ typedef struct {
   int32_t d;            /* query/key head dim, positive multiple of 4         */
   int32_t dv;           /* value head dim, positive multiple of 4             */
   int32_t rect;         /* nys_rect                                           */
+  int32_t exact_cap;    /* keys an exact-only (short-prompt) group can hold; 0
+                           (the default) refuses such prompts.  See nys_seal. */
 } nys_config;
 
 typedef struct nys_states nys_states; /* opaque host handle */
@@ -100,9 +103,12 @@ typedef struct nys_states nys_states; /* opaque host handle */
  *   m_max   f32 [G][H][m]        per-landmark running max of far logits
  *   t_lo    bf16 [G][H][m][dv]   low part of the far numerator
  *   z_lo    f32 [G][H][m]        low part of the far denominator
+ *   exact_k f32 [G][exact_cap][d]   keys of exact-only groups (absent if 0)
+ *   exact_v f32 [G][exact_cap][dv]  their values
  *   far_len i32 [G][H]           keys absorbed per head
  *   ints    i32 [G][8]           {win_head, win_len, m_eff, t, mode, status, 0, 0},
- *                                mode 0 = empty, 1 = sealed (landmark path);
+ *                                mode 0 = empty, 1 = sealed (landmark path),
+ *                                2 = sealed exact-only (win_len = keys held);
  *                                status 0 = fine, nonzero = a bounded wait in a
  *                                decode kernel gave up (every wait is limited
  *                                to 2 s); that group's state is then invalid
@@ -121,6 +127,7 @@ typedef struct {
   size_t off_q_tilde, off_mu, off_t_hat, off_z_hat, off_m_max;
   size_t off_t_lo, off_z_lo;
   size_t off_far_len, off_ints;
+  size_t off_exact_k, off_exact_v;
   int64_t n_groups;
   int32_t ints_per_group; /* 8 */
 } nys_layout;
@@ -172,6 +179,13 @@ int nys_free_states(nys_states* st);
  *    ring, keys sink..t-w-1 are in every head's far field with per-landmark
  *    running max, far_len = t - sink - w.
  * Inputs: q [n][heads_per_kv][t][d], k [n][t][d], v [n][t][dv] (device).
+ * Short prompts, t <= w + sink + 8, take the page's exact-only mode
+ * (nystrom.rs, prefill_shared and seal_exact): every key stays an exact key
+ * in a growing window, with no sinks, landmarks or far field; each decode
+ * token appends its key and attends over all keys so far.  That needs
+ * cfg.exact_cap >= t (else NYS_E_EXACT_ONLY when exact_cap is 0, NYS_E_RANGE
+ * when t > exact_cap); nys_step_batch returns NYS_E_CAPACITY before a token
+ * that would exceed exact_cap keys.
  * All n groups share t.  Re-sealing a group replaces its state.  Allocates a
  * temporary f64 workspace of n*m*d*8 bytes with cudaMallocAsync on `stream`
  * and frees it there.  Writes no attention output (the page's prefill
@@ -205,8 +219,9 @@ int nys_seal_ragged(nys_states* st, int64_t g0, int64_t n, const int32_t* t_host
  * every head's output.
  * Inputs: q [n][heads_per_kv][d], k [n][d], v [n][dv]; output
  * out [n][heads_per_kv][dv] (all device).  One kernel launch.
+ * Groups sealed in exact-only mode run a second, exact-attention kernel.
  * Errors: NYS_E_INVAL, NYS_E_RANGE, NYS_E_NOT_SEALED, NYS_E_ALIGN,
- * NYS_E_CUDA. */
+ * NYS_E_CAPACITY, NYS_E_CUDA. */
 int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
                    const float* k, const float* v, float* out, void* stream);
 

@@ -19,6 +19,8 @@ struct nys_states {
   bool owned;
   nys_layout lay;
   std::vector<uint8_t> sealed;  // host record of groups with a sealed state
+  std::vector<int32_t> exact_len;  // keys held by exact-only groups, -1 otherwise
+  int64_t n_exact;                 // how many groups are exact-only
   int device;
 };
 
@@ -36,6 +38,8 @@ int check_config(const nys_config* c) {
   if (c->m < 4 || c->w < 1 || c->sink < 0 || c->heads_per_kv < 1) return NYS_E_INVAL;
   if (c->d <= 0 || c->dv <= 0 || (c->d & 3) || (c->dv & 3)) return NYS_E_INVAL;
   if (c->rect != NYS_RECT_AGGREGATE && c->rect != NYS_RECT_FM) return NYS_E_INVAL;
+  if (c->exact_cap < 0) return NYS_E_INVAL;
+  if (c->exact_cap > nys::kMaxExactCap) return NYS_E_UNSUPPORTED;
   if (c->m > nys::kMaxM || c->d > nys::kMaxDim || c->dv > nys::kMaxDim ||
       c->heads_per_kv > nys::kMaxHeads || (int64_t)c->sink + c->w > nys::kMaxNear)
     return NYS_E_UNSUPPORTED;
@@ -72,6 +76,8 @@ bool make_layout(const nys_config& c, int64_t G, nys_layout* L) {
   L->off_z_lo = region(g * H * m * 4);
   L->off_far_len = region(g * H * 4);
   L->off_ints = region(g * nys::kIntsPerGroup * 4);
+  L->off_exact_k = region(g * (size_t)c.exact_cap * c.d * 4);
+  L->off_exact_v = region(g * (size_t)c.exact_cap * c.dv * 4);
   L->total_bytes = o;
   L->n_groups = G;
   L->ints_per_group = nys::kIntsPerGroup;
@@ -96,6 +102,9 @@ nys::DevState dev_state(const nys_states* st) {
   s.z_lo = reinterpret_cast<float*>(b + L.off_z_lo);
   s.far_len = reinterpret_cast<int32_t*>(b + L.off_far_len);
   s.ints = reinterpret_cast<int32_t*>(b + L.off_ints);
+  s.exact_k = reinterpret_cast<float*>(b + L.off_exact_k);
+  s.exact_v = reinterpret_cast<float*>(b + L.off_exact_v);
+  s.exact_cap = st->cfg.exact_cap;
   s.m = st->cfg.m;
   s.w = st->cfg.w;
   s.sink = st->cfg.sink;
@@ -115,6 +124,17 @@ int check_range(const nys_states* st, int64_t g0, int64_t n) {
 }
 
 std::atomic<bool> g_clamp_said{false};
+
+// Host record: groups [g0, g0+n) now hold landmark-path states.
+void forget_exact(nys_states* st, int64_t g0, int64_t n) {
+  if (!st->n_exact) return;
+  for (int64_t g = g0; g < g0 + n; ++g) {
+    if (st->exact_len[(size_t)g] >= 0) {
+      st->exact_len[(size_t)g] = -1;
+      --st->n_exact;
+    }
+  }
+}
 
 }  // namespace
 
@@ -145,6 +165,7 @@ int prepare_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* 
 
 void record_sealed(nys_states* st, int64_t g0, int64_t n) {
   if (n > 0) std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  forget_exact(st, g0, n);
 }
 
 }  // namespace nys
@@ -164,6 +185,8 @@ const char* nys_strerror(int status) {
     case NYS_E_CUDA: return "CUDA error";
     case NYS_E_UNSUPPORTED:
       return "geometry beyond kernel limits (m <= 64, d, dv <= 256, heads <= 64, sink + w <= 2048)";
+    case NYS_E_CAPACITY:
+      return "an exact-only group would hold more than exact_cap keys";
     case NYS_E_SCRATCH:
       return "one group's seal workspace, (1 + heads_per_kv) * m * d * 8 bytes, exceeds the "
              "4 MiB static scratch of nys_seal_static; use nys_seal";
@@ -221,6 +244,8 @@ int nys_alloc_states(const nys_config* cfg, int64_t n_groups, void* dev_buf,
     return NYS_E_CUDA;
   }
   st->sealed.assign((size_t)n_groups, 0);
+  st->exact_len.assign((size_t)n_groups, -1);
+  st->n_exact = 0;
   *out = st;
   return NYS_OK;
 }
@@ -240,8 +265,24 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
   if (rc) return rc;
   const nys_config& c = st->cfg;
   if (t < 1) return NYS_E_RANGE;
-  // nystrom.rs, prefill_shared: short prompts skip the skeleton entirely.
-  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) return NYS_E_EXACT_ONLY;
+  // nystrom.rs, prefill_shared: short prompts skip the skeleton entirely and
+  // keep every key exact (exact-only mode), which needs the exact region.
+  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) {
+    if (c.exact_cap == 0) return NYS_E_EXACT_ONLY;
+    if (t > c.exact_cap) return NYS_E_RANGE;
+    if (n == 0) return NYS_OK;
+    if (!k || !v) return NYS_E_INVAL;
+    if (!aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
+    if (nys::launch_exact_seal(dev_state(st), g0, n, t, k, v,
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return NYS_E_CUDA;
+    std::memset(st->sealed.data() + g0, 1, (size_t)n);
+    for (int64_t g = g0; g < g0 + n; ++g) {
+      if (st->exact_len[(size_t)g] < 0) ++st->n_exact;
+      st->exact_len[(size_t)g] = t;
+    }
+    return NYS_OK;
+  }
   if (n == 0) return NYS_OK;
   if (!q || !k || !v) return NYS_E_INVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
@@ -268,9 +309,10 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
                          k + a * (int64_t)t * c.d, v + a * (int64_t)t * c.dv,
                          static_cast<double*>(ws), s);
   }
-  cudaError_t ef = cudaFreeAsync(ws, s);
+  const cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess || ef != cudaSuccess) return NYS_E_CUDA;
   std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  forget_exact(st, g0, n);
   return NYS_OK;
 }
 
@@ -341,6 +383,7 @@ int nys_seal_ragged(nys_states* st, int64_t g0, int64_t n, const int32_t* t_host
   // The host arrays above were staged by the copies before they returned.
   if (e != cudaSuccess || f1 != cudaSuccess || f2 != cudaSuccess) return NYS_E_CUDA;
   std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  forget_exact(st, g0, n);
   return NYS_OK;
 }
 
@@ -353,10 +396,24 @@ int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
   if (!q || !k || !v || !out) return NYS_E_INVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NYS_E_ALIGN;
   if (std::memchr(st->sealed.data() + g0, 0, (size_t)n)) return NYS_E_NOT_SEALED;
+  int64_t exact_here = 0;
+  if (st->n_exact) {
+    for (int64_t g = g0; g < g0 + n; ++g) {
+      const int32_t len = st->exact_len[(size_t)g];
+      if (len < 0) continue;
+      if (len >= st->cfg.exact_cap) return NYS_E_CAPACITY;
+      ++exact_here;
+    }
+  }
   const nys::DevState ds = dev_state(st);
-  if (nys::launch_step(ds, g0, n, q, k, v, out, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (exact_here < n && nys::launch_step(ds, g0, n, q, k, v, out, s) != cudaSuccess)
     return NYS_E_CUDA;
+  if (exact_here) {
+    if (nys::launch_exact_step(ds, g0, n, q, k, v, out, s) != cudaSuccess) return NYS_E_CUDA;
+    for (int64_t g = g0; g < g0 + n; ++g)
+      if (st->exact_len[(size_t)g] >= 0) ++st->exact_len[(size_t)g];
+  }
   return NYS_OK;
 }
 
@@ -395,6 +452,7 @@ int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n) {
   int rc = check_range(st, g0, n);
   if (rc) return rc;
   if (n) std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  forget_exact(st, g0, n);
   return NYS_OK;
 }
 

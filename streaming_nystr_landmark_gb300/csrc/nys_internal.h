@@ -43,7 +43,8 @@ enum : int {
   kIntStatus = 5,  // nonzero: a bounded wait in the step kernel gave up
   kIntsPerGroup = 8
 };
-enum : int { kModeEmpty = 0, kModeSealed = 1 };
+enum : int { kModeEmpty = 0, kModeSealed = 1, kModeExact = 2 };
+constexpr int kMaxExactCap = 4096;
 
 // Device pointers of every state region plus the geometry, passed by value
 // to the kernels.  Region layout: see nys_layout in nys.h.
@@ -62,7 +63,9 @@ struct DevState {
   float* z_lo;     // low part of z_hat
   int32_t* far_len;
   int32_t* ints;
-  int32_t m, w, sink, heads, d, dv, rect;
+  float* exact_k;  // [G][exact_cap][d], exact-only groups
+  float* exact_v;  // [G][exact_cap][dv]
+  int32_t m, w, sink, heads, d, dv, rect, exact_cap;
   float scale;  // 1/sqrt(d) evaluated in f32
 };
 
@@ -183,6 +186,14 @@ __device__ __forceinline__ void seal_geom(const SealGeom& sg, int64_t gi, int& t
   }
 }
 #endif
+
+// Exact-only (short-prompt) groups: copy the prompt into the exact region and
+// set the counters (seal), and one decode token of exact softmax attention over
+// every key held (step; groups in other modes are left alone).
+cudaError_t launch_exact_seal(const DevState& s, int64_t g0, int64_t n, int t, const float* k,
+                              const float* v, cudaStream_t stream);
+cudaError_t launch_exact_step(const DevState& s, int64_t g0, int64_t n, const float* q,
+                              const float* k, const float* v, float* out, cudaStream_t stream);
 
 // Bytes of f64 workspace the seal needs per group (key landmarks and every
 // head's query landmarks before rounding).

@@ -124,6 +124,7 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
   float* part = sm + L.part;
 
   int32_t* ints = s.ints + g * kIntsPerGroup;
+  if (ints[kIntMode] == kModeExact) return;  // exact-only groups: nys_exact.cu
   const int win_head = ints[kIntWinHead];
   const int win_len = ints[kIntWinLen];
   const int m_eff = ints[kIntMEff];

@@ -209,21 +209,24 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     bool ok = true;
     // The ring slot of the next group is read one group ahead so that the
     // load's latency overlaps the current group's copies.
-    int2 nxt = make_int2(0, 0);
+    int3 nxt = make_int3(0, 0, 0);
     if (blockIdx.x < n) {
       const int32_t* ints0 = s.ints + (g0 + blockIdx.x) * kIntsPerGroup;
-      nxt = make_int2(ints0[kIntWinHead], ints0[kIntWinLen]);
+      nxt = make_int3(ints0[kIntWinHead], ints0[kIntWinLen], ints0[kIntMode]);
     }
     for (int64_t gi = blockIdx.x; gi < n && ok; gi += gridDim.x) {
       const int64_t g = g0 + gi;
       const int32_t* ints = s.ints + g * kIntsPerGroup;
       int slot = (nxt.y == w) ? nxt.x : nxt.y;
       slot = min(max(slot, 0), w - 1);
+      // Exact-only groups (a separate kernel steps them) take only the misc
+      // stage, from which the consumers learn to skip them.
+      const int stages = (nxt.z == kModeExact) ? 1 : P.per_group;
       if (gi + gridDim.x < n) {
         const int32_t* in2 = s.ints + (g + gridDim.x) * kIntsPerGroup;
-        nxt = make_int2(in2[kIntWinHead], in2[kIntWinLen]);
+        nxt = make_int3(in2[kIntWinHead], in2[kIntWinLen], in2[kIntMode]);
       }
-      for (int st = 0; st < P.per_group && ok;
+      for (int st = 0; st < stages && ok;
            ++st, ++c, idx = (idx + 1 == S) ? 0 : idx + 1, phase ^= (idx == 0) ? 1u : 0u) {
         if (!wait_bar(&empty[idx], phase ^ 1u, abort)) {
           ok = false;
@@ -377,6 +380,11 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     release_slot(ci);
     advance();
     if (!csync()) { fail(g); return; }
+    if (xints[kIntMode] == kModeExact) {
+      // every thread has read the mode before the next group's misc copy
+      if (!csync()) { fail(g); return; }
+      continue;
+    }
     const int win_head = xints[kIntWinHead];
     const int win_len = xints[kIntWinLen];
     const int m_eff = min(max(xints[kIntMEff], 0), m);

@@ -25,6 +25,7 @@ NYS_E_ALIGN = -6
 NYS_E_CUDA = -7
 NYS_E_UNSUPPORTED = -8
 NYS_E_SCRATCH = -9
+NYS_E_CAPACITY = -10
 NYS_RECT_AGGREGATE = 0
 NYS_RECT_FM = 1
 
@@ -39,7 +40,7 @@ class NysConfig(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("w", ctypes.c_int32),
                 ("sink", ctypes.c_int32), ("heads_per_kv", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("dv", ctypes.c_int32),
-                ("rect", ctypes.c_int32)]
+                ("rect", ctypes.c_int32), ("exact_cap", ctypes.c_int32)]
 
 
 class NysLayout(ctypes.Structure):
@@ -51,6 +52,7 @@ class NysLayout(ctypes.Structure):
                 ("off_z_hat", ctypes.c_size_t), ("off_m_max", ctypes.c_size_t),
                 ("off_t_lo", ctypes.c_size_t), ("off_z_lo", ctypes.c_size_t),
                 ("off_far_len", ctypes.c_size_t), ("off_ints", ctypes.c_size_t),
+                ("off_exact_k", ctypes.c_size_t), ("off_exact_v", ctypes.c_size_t),
                 ("n_groups", ctypes.c_int64), ("ints_per_group", ctypes.c_int32)]
 
 
@@ -106,8 +108,9 @@ def nys_strerror(code: int) -> str:
     return _lib.nys_strerror(code).decode()
 
 
-def make_config(m, w, sink, heads_per_kv, d, dv, rect=NYS_RECT_AGGREGATE) -> NysConfig:
-    return NysConfig(m, w, sink, heads_per_kv, d, dv, rect)
+def make_config(m, w, sink, heads_per_kv, d, dv, rect=NYS_RECT_AGGREGATE,
+                exact_cap=0) -> NysConfig:
+    return NysConfig(m, w, sink, heads_per_kv, d, dv, rect, exact_cap)
 
 
 def nys_memory_bytes(cfg: NysConfig, n_groups: int) -> int:
@@ -197,10 +200,10 @@ class NystromStates:
     """A batch of group states in one torch-owned device buffer."""
 
     def __init__(self, m, w, sink, heads_per_kv, d, dv, n_groups,
-                 rect=NYS_RECT_AGGREGATE, device="cuda"):
+                 rect=NYS_RECT_AGGREGATE, device="cuda", exact_cap=0):
         import torch
         self.torch = torch
-        self.cfg = make_config(m, w, sink, heads_per_kv, d, dv, rect)
+        self.cfg = make_config(m, w, sink, heads_per_kv, d, dv, rect, exact_cap)
         self.n_groups = n_groups
         self.device = torch.device(device)
         nbytes = nys_memory_bytes(self.cfg, n_groups)
@@ -296,6 +299,8 @@ class NystromStates:
             "z_lo": (torch.float32, (G, H, m)),
             "far_len": (torch.int32, (G, H)),
             "ints": (torch.int32, (G, self.layout.ints_per_group)),
+            "exact_k": (torch.float32, (G, c.exact_cap, c.d)),
+            "exact_v": (torch.float32, (G, c.exact_cap, c.dv)),
         }
         dtype, shape = shapes[name]
         off = getattr(self.layout, "off_" + name) + self._off

@@ -30,16 +30,18 @@ def _align(x):
     return (x + 255) // 256 * 256
 
 
-@pytest.mark.parametrize("geo", [(32, 128, 4, 2, 128, 128, 14336),
-                                 (8, 16, 4, 1, 64, 64, 1),
-                                 (64, 128, 4, 8, 128, 128, 512),
-                                 (5, 3, 0, 3, 12, 20, 7)])
+@pytest.mark.parametrize("geo", [(32, 128, 4, 2, 128, 128, 14336, 0),
+                                 (8, 16, 4, 1, 64, 64, 1, 0),
+                                 (64, 128, 4, 8, 128, 128, 512, 0),
+                                 (5, 3, 0, 3, 12, 20, 7, 0),
+                                 (8, 16, 4, 2, 32, 32, 9, 100)])
 def test_memory_bytes_matches_documented_layout(geo):
-    m, w, sink, H, d, dv, G = geo
-    cfg = nys.make_config(m, w, sink, H, d, dv)
+    m, w, sink, H, d, dv, G, cap = geo
+    cfg = nys.make_config(m, w, sink, H, d, dv, exact_cap=cap)
     sizes = [G * w * d, G * w * dv, G * sink * d, G * sink * dv, G * m * d,
              G * H * m * d, G * H * m * m, G * H * m * dv, G * H * m, G * H * m,
-             G * H * m * dv / 2, G * H * m, G * H, G * 8]   # t_lo is bf16
+             G * H * m * dv / 2, G * H * m, G * H, G * 8,   # t_lo is bf16
+             G * cap * d, G * cap * dv]
     want = sum(_align(int(4 * s)) for s in sizes)
     assert nys.nys_memory_bytes(cfg, G) == want
 
@@ -65,6 +67,8 @@ def test_memory_line_shares_window_across_heads():
     ((32, 128, 4, 2, 260, 128), nys.NYS_E_UNSUPPORTED),
     ((32, 128, 4, 65, 128, 128), nys.NYS_E_UNSUPPORTED),
     ((32, 2045, 4, 2, 128, 128), nys.NYS_E_UNSUPPORTED),
+    ((32, 128, 4, 2, 128, 128, 0, -1), nys.NYS_E_INVAL),      # negative exact_cap
+    ((32, 128, 4, 2, 128, 128, 0, 4097), nys.NYS_E_UNSUPPORTED),
 ])
 def test_bad_geometry_rejected(bad, code):
     with pytest.raises(nys.NysError) as ei:
