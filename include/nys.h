@@ -272,6 +272,59 @@ int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n);
 /* The geometry a handle was created with.  Errors: NYS_E_INVAL. */
 int nys_config_of(const nys_states* st, nys_config* cfg, int64_t* n_groups);
 
+/* ---- One layer's O(1) override over a batch of sequences ------------------
+ * The lifecycle of Struct LayerKvCache (o1_begin, o1_push_q, o1_sealed,
+ * o1_seal, o1_step, o1_views, o1_memory_bytes) on top of the calls above.
+ * A layer has num_heads query heads over num_kv_heads KV heads for each of
+ * `batch` sequences; query head h of a sequence belongs to KV group
+ * h / (num_heads / num_kv_heads), so q/out rows are [batch][num_heads][d]. */
+typedef struct nys_o1 nys_o1; /* opaque */
+
+/* Arm query collection for a fresh prompt pass (o1_begin): cfg gives m, w,
+ * sink, rect, d, dv and exact_cap (heads_per_kv is ignored: it is fixed at
+ * seal time from the fan-out).  Allocates a device query trace of
+ * batch*num_heads*max_prompt*d floats.  Errors: NYS_E_INVAL,
+ * NYS_E_UNSUPPORTED, NYS_E_CUDA. */
+int nys_o1_begin(const nys_config* cfg, int32_t batch, int32_t num_heads,
+                 int32_t num_kv_heads, int32_t max_prompt, nys_o1** out);
+
+/* Record one prompt position's queries of every sequence (o1_push_q):
+ * q_all [batch][num_heads][d] (device), one strided copy on `stream`.  A
+ * no-op once the layer is sealed; NYS_E_RANGE after max_prompt positions. */
+int nys_o1_push_q(nys_o1* o, const float* q_all, void* stream);
+
+/* Freeze the prompt (o1_seal): k [batch][num_kv_heads][kv_len][d] and v
+ * [..][dv] are the layer's prompt keys/values (device, f32).  *sealed = 1
+ * when the states were built -- the caller may then drop its KV for this
+ * layer; *sealed = 0 (status NYS_OK) when a precondition of the page fails
+ * and the layer must stay exact: the query trace is not complete (positions
+ * pushed != kv_len), the GQA fan-out does not divide, the KV is not densely
+ * stored (kv_dense = 0), or a short prompt (kv_len <= w + sink + 8) has no
+ * exact_cap room.  Synchronises `stream`, then releases the trace.
+ * Errors: those of nys_alloc_states and nys_seal. */
+int nys_o1_seal(nys_o1* o, const float* k, const float* v, int32_t kv_len,
+                int32_t kv_dense, void* stream, int32_t* sealed);
+
+/* *sealed = 1 once nys_o1_seal built the states (o1_sealed). */
+int nys_o1_sealed(const nys_o1* o, int32_t* sealed);
+
+/* One decode token of the whole layer (o1_step): q_all [batch][num_heads][d],
+ * k_new/v_new [batch][num_kv_heads][d|dv], out [batch][num_heads][dv].
+ * Errors: NYS_E_NOT_SEALED, and those of nys_step_batch. */
+int nys_o1_step(nys_o1* o, const float* q_all, const float* k_new,
+                const float* v_new, float* out, void* stream);
+
+/* Device bytes held (o1_memory_bytes): the query trace recorded so far while
+ * collecting, the states once sealed. */
+int nys_o1_memory_bytes(const nys_o1* o, size_t* bytes);
+
+/* The sealed states (the o1_views analogue; see nys_layout_of), or
+ * NYS_E_NOT_SEALED.  Owned by the nys_o1. */
+int nys_o1_states(const nys_o1* o, nys_states** st);
+
+/* Release the trace and the states.  NULL is a no-op. */
+int nys_o1_free(nys_o1* o);
+
 /* Static description of a status code.  Never NULL. */
 const char* nys_strerror(int status);
 

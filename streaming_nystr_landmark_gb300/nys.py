@@ -33,7 +33,9 @@ NYS_RECT_FM = 1
 EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
             "nys_seal", "nys_step_batch", "nys_query", "nys_layout_of",
             "nys_mark_sealed", "nys_config_of", "nys_strerror",
-            "nys_seal_static", "nys_seal_ragged")
+            "nys_seal_static", "nys_seal_ragged", "nys_o1_begin", "nys_o1_push_q",
+            "nys_o1_seal", "nys_o1_sealed", "nys_o1_step", "nys_o1_memory_bytes",
+            "nys_o1_states", "nys_o1_free")
 
 
 class NysConfig(ctypes.Structure):
@@ -82,6 +84,14 @@ def _load():
         "nys_strerror": [ctypes.c_int],
         "nys_seal_static": [VP, I64, I64, I32, VP, VP, VP, VP],
         "nys_seal_ragged": [VP, I64, I64, P(I32), VP, VP, VP, VP],
+        "nys_o1_begin": [P(NysConfig), I32, I32, I32, I32, P(VP)],
+        "nys_o1_push_q": [VP, VP, VP],
+        "nys_o1_seal": [VP, VP, VP, I32, I32, VP, P(I32)],
+        "nys_o1_sealed": [VP, P(I32)],
+        "nys_o1_step": [VP, VP, VP, VP, VP, VP],
+        "nys_o1_memory_bytes": [VP, P(ctypes.c_size_t)],
+        "nys_o1_states": [VP, P(VP)],
+        "nys_o1_free": [VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -378,3 +388,73 @@ class HostPipeline:
 
     def synchronize(self):
         self.torch.cuda.synchronize(self.st.device)
+
+
+class O1Layer:
+    """One attention layer's O(1) override for a batch of sequences (the
+    LayerKvCache o1 lifecycle: begin -> push_q per prompt position -> seal ->
+    step per decode token), over the nys_o1_* calls."""
+
+    def __init__(self, m, w, sink, d, dv, batch, num_heads, num_kv_heads, max_prompt,
+                 rect=NYS_RECT_AGGREGATE, exact_cap=0, device="cuda"):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device)
+        self.cfg = make_config(m, w, sink, 1, d, dv, rect, exact_cap)
+        self.batch, self.num_heads, self.num_kv = batch, num_heads, num_kv_heads
+        h = ctypes.c_void_p(0)
+        _check(_lib.nys_o1_begin(ctypes.byref(self.cfg), batch, num_heads, num_kv_heads,
+                                 max_prompt, ctypes.byref(h)), "nys_o1_begin")
+        self.handle = h.value
+
+    def _stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def push_q(self, q_all):
+        c = self.cfg
+        _check(_lib.nys_o1_push_q(self.handle, _ptr(q_all, self.torch.float32,
+                                                    (self.batch, self.num_heads, c.d), "q_all"),
+                                  self._stream()), "nys_o1_push_q")
+
+    def seal(self, k, v, kv_dense=True):
+        """k [batch][num_kv][t][d], v [..][dv]; True when sealed."""
+        c = self.cfg
+        t = k.shape[2]
+        flag = ctypes.c_int32(0)
+        _check(_lib.nys_o1_seal(
+            self.handle,
+            _ptr(k, self.torch.float32, (self.batch, self.num_kv, t, c.d), "k"),
+            _ptr(v, self.torch.float32, (self.batch, self.num_kv, t, c.dv), "v"),
+            t, int(bool(kv_dense)), self._stream(), ctypes.byref(flag)), "nys_o1_seal")
+        return bool(flag.value)
+
+    def sealed(self):
+        flag = ctypes.c_int32(0)
+        _check(_lib.nys_o1_sealed(self.handle, ctypes.byref(flag)), "nys_o1_sealed")
+        return bool(flag.value)
+
+    def step(self, q_all, k_new, v_new, out):
+        c, f = self.cfg, self.torch.float32
+        _check(_lib.nys_o1_step(
+            self.handle, _ptr(q_all, f, (self.batch, self.num_heads, c.d), "q_all"),
+            _ptr(k_new, f, (self.batch, self.num_kv, c.d), "k_new"),
+            _ptr(v_new, f, (self.batch, self.num_kv, c.dv), "v_new"),
+            _ptr(out, f, (self.batch, self.num_heads, c.dv), "out"), self._stream()),
+            "nys_o1_step")
+        return out
+
+    def memory_bytes(self):
+        out = ctypes.c_size_t(0)
+        _check(_lib.nys_o1_memory_bytes(self.handle, ctypes.byref(out)), "nys_o1_memory_bytes")
+        return out.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check(_lib.nys_o1_free(self.handle), "nys_o1_free")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

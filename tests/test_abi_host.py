@@ -15,7 +15,7 @@ nys = pytest.importorskip("streaming_nystr_landmark_gb300.nys")
 def _declared():
     text = open(os.path.join(ROOT, "include", "nys.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return set(re.findall(r"\b(nys_[a-z_]+)\s*\(", text))
+    return set(re.findall(r"\b(nys_[a-z0-9_]+)\s*\(", text))
 
 
 def test_every_declared_symbol_is_exported():

@@ -1,0 +1,104 @@
+"""The LayerKvCache o1 lifecycle (nys_o1_*): collect the prompt's queries one
+position at a time, seal when the page's preconditions hold, then decode.
+
+A layer sealed through the lifecycle must hold exactly the states a direct
+nys_seal of the same groups builds, and decode identically; every failed
+precondition must leave the layer unsealed (exact), as o1_seal returns false."""
+import numpy as np
+import pytest
+
+from streaming_nystr_landmark_gb300 import nys
+from streaming_nystr_landmark_gb300.workloads import Workload, host_prompt_batch, host_token_batch
+
+pytestmark = pytest.mark.gpu
+
+B, NH, NKV, D, M, W, SINK, T = 3, 4, 2, 32, 8, 16, 4, 64
+HPK = NH // NKV
+
+
+def _inputs(cuda_device):
+    import torch
+    wl = Workload("o1", HPK, D, D, M, W, SINK, 0, T, 8, 1, 1, B * NKV, "unit2", seed=51)
+    q, k, v, gens = host_prompt_batch(wl, range(B * NKV))   # groups g = b*NKV + kvh
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(cuda_device)
+    # the layer's view: q_all[pos] = [B][NH][D], head h of sequence b is
+    # query head h % HPK of group b*NKV + h // HPK
+    q_layer = q.reshape(B, NKV, HPK, T, D).reshape(B, NH, T, D)
+    return wl, gens, dev, q, k, v, q_layer
+
+
+def test_lifecycle_matches_direct_seal_and_decode(cuda_device):
+    import torch
+    wl, gens, dev, q, k, v, q_layer = _inputs(cuda_device)
+    layer = nys.O1Layer(M, W, SINK, D, D, B, NH, NKV, max_prompt=100, device=cuda_device)
+    with pytest.raises(nys.NysError) as ei:
+        layer.step(*[torch.zeros(s, device=cuda_device) for s in
+                     ((B, NH, D), (B, NKV, D), (B, NKV, D), (B, NH, D))])
+    assert ei.value.code == nys.NYS_E_NOT_SEALED
+    for p in range(T):
+        layer.push_q(dev(q_layer[:, :, p, :]))
+    assert layer.memory_bytes() == B * NH * T * D * 4          # the trace so far
+    assert not layer.sealed()
+    assert layer.seal(dev(k.reshape(B, NKV, T, D)), dev(v.reshape(B, NKV, T, D)))
+    assert layer.sealed()
+    direct = nys.NystromStates(M, W, SINK, HPK, D, D, B * NKV, 0, cuda_device)
+    direct.seal(dev(q), dev(k), dev(v))
+    assert layer.memory_bytes() == nys.nys_memory_bytes(direct.cfg, B * NKV)
+    layer.push_q(dev(q_layer[:, :, 0, :]))                     # no-op once sealed
+    # the layer's states are the direct states, byte for byte
+    import ctypes
+    sp = ctypes.c_void_p(0)
+    assert nys._lib.nys_o1_states(layer.handle, ctypes.byref(sp)) == 0
+    base, lay = nys.nys_layout_of(sp.value)
+    torch.cuda.synchronize()
+
+    class _Raw:  # a view of the library-owned state buffer
+        def __init__(self, ptr, n):
+            self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1",
+                                             "data": (ptr, False), "version": 2}
+
+    ours = torch.as_tensor(_Raw(base, lay.total_bytes), device=cuda_device)
+    theirs = direct.buf[direct._off:direct._off + lay.total_bytes]
+    assert torch.equal(ours, theirs)
+    for n in range(8):
+        tq, tk, tv = host_token_batch(gens, n)                   # per group
+        q_all = dev(tq.reshape(B, NKV, HPK, D).reshape(B, NH, D))
+        kn, vn = dev(tk.reshape(B, NKV, D)), dev(tv.reshape(B, NKV, D))
+        out_l = torch.empty((B, NH, D), device=cuda_device)
+        layer.step(q_all, kn, vn, out_l)
+        out_d = torch.empty((B * NKV, HPK, D), device=cuda_device)
+        direct.step(dev(tq), dev(tk), dev(tv), out_d)
+        assert torch.equal(out_l.reshape(-1), out_d.reshape(-1)), n
+    layer.close()
+    direct.close()
+
+
+@pytest.mark.parametrize("case", ["fan_out", "short_trace", "not_dense", "no_exact_room"])
+def test_failed_preconditions_keep_the_layer_exact(cuda_device, case):
+    wl, gens, dev, q, k, v, q_layer = _inputs(cuda_device)
+    nh, t = (3 if case == "fan_out" else NH), T
+    kk, vv = k, v
+    if case == "no_exact_room":
+        t = 20                                                   # <= w + sink + 8
+        kk, vv = k[:, :t], v[:, :t]
+    layer = nys.O1Layer(M, W, SINK, D, D, B, nh, NKV, max_prompt=100, device=cuda_device)
+    pushes = t - 1 if case == "short_trace" else t
+    for p in range(pushes):
+        layer.push_q(dev(np.ascontiguousarray(q_layer[:, :nh, p, :])))
+    ok = layer.seal(dev(kk.reshape(B, NKV, t, D)), dev(vv.reshape(B, NKV, t, D)),
+                    kv_dense=(case != "not_dense"))
+    assert not ok and not layer.sealed()
+    assert layer.memory_bytes() == B * nh * pushes * D * 4       # trace kept
+    layer.close()
+
+
+def test_trace_capacity(cuda_device):
+    import torch
+    layer = nys.O1Layer(M, W, SINK, D, D, 1, 2, 1, max_prompt=3, device=cuda_device)
+    z = torch.zeros((1, 2, D), device=cuda_device)
+    for _ in range(3):
+        layer.push_q(z)
+    with pytest.raises(nys.NysError) as ei:
+        layer.push_q(z)
+    assert ei.value.code == nys.NYS_E_RANGE
+    layer.close()
