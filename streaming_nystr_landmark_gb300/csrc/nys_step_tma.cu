@@ -34,14 +34,13 @@ namespace {
 constexpr int kCWarps = 8;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kThreadsTma = kCThreads + 32;
-constexpr int kStageBytes = 16384;
 constexpr int kMaxRing = 12;
 constexpr int kRowsPerRound = 4;
 constexpr uint64_t kWaitNs = 2000000000ull;  // every wait gives up after 2 s
 constexpr uint32_t kSuspendNs = 1000000;      // a waiting thread sleeps up to 1 ms per try
 constexpr int kSmemBudget = 227 * 1024;    // one CTA per SM
 constexpr int kSmemBudget2 = 113 * 1024;   // each of two CTAs per SM
-constexpr int kMinRing2 = 5;
+constexpr int kMinRing = 3;
 
 __host__ __device__ inline int r4(int x) { return (x + 3) & ~3; }
 
@@ -58,6 +57,7 @@ struct TmaPlan {
   int x_sig, x_fh, x_lg, x_rs, x_es, x_gs, x_zs, x_ms, x_den, x_fl, x_ints, x_part;
   int nrp, mp, scratch_floats;
   int ring;
+  int stage_bytes;  // 32 KB when the ring still fits, else 16 KB
   int ctas_per_sm;
   int ring_off;  // bytes from the smem base to the ring
   size_t smem_bytes;
@@ -183,7 +183,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   uint64_t* cbar = empty + kMaxRing;
   int* abort = reinterpret_cast<int*>(cbar + 1);
   unsigned char* ring = smem + P.ring_off;
-  float* X = reinterpret_cast<float*>(ring + (size_t)P.ring * kStageBytes);
+  float* X = reinterpret_cast<float*>(ring + (size_t)P.ring * P.stage_bytes);
 
   const int d = s.d, dv = s.dv, w = s.w, ns = s.sink, H = s.heads, m = s.m;
   const int d4 = d >> 2, S = P.ring;
@@ -232,7 +232,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           ok = false;
           break;
         }
-        unsigned char* dst = ring + (size_t)idx * kStageBytes;
+        unsigned char* dst = ring + (size_t)idx * P.stage_bytes;
         uint64_t* bar = &full[idx];
         if (st == 0) {
           mbar_expect_tx(bar, (uint32_t)P.misc_bytes);
@@ -334,7 +334,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       cpar ^= 1u;
     }
   };
-  auto stage_ptr = [&](int i) { return ring + (size_t)i * kStageBytes; };
+  auto stage_ptr = [&](int i) { return ring + (size_t)i * P.stage_bytes; };
   auto release_slot = [&](int i) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[i]);
@@ -778,17 +778,16 @@ cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64
 // Plan the stage layout; false when the geometry is outside this kernel
 // (every bulk copy must start and end on 16 bytes, dv <= 128, H <= 8, and the
 // misc stage and the scratch must fit).
-bool plan_step_tma(const DevState& s, void* plan_out) {
-  TmaPlan& P = *static_cast<TmaPlan*>(plan_out);
+// Plan one stage size and CTA count; false if it does not fit.
+static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P) {
   const int d = s.d, dv = s.dv, m = s.m, H = s.heads, w = s.w, ns = s.sink;
-  if (H > 8 || d > 128 || dv > 128 || (dv & 7) || (d & 3) || ((H * m) & 3) || (m & 3))
-    return false;
   const int ht = H <= 1 ? 1 : H <= 2 ? 2 : H <= 4 ? 4 : 8;
-  P.rows_k = kStageBytes / (d * 4);
-  P.rows_m = kStageBytes / (m * 4);
+  P.stage_bytes = stage_bytes;
+  P.rows_k = stage_bytes / (d * 4);
+  P.rows_m = stage_bytes / (m * 4);
   if (P.rows_m % m) return false;  // a head's M block must not straddle stages
-  P.rows_v = kStageBytes / (dv * 4);
-  P.rows_t = kStageBytes / (dv * 6);
+  P.rows_v = stage_bytes / (dv * 4);
+  P.rows_t = stage_bytes / (dv * 6);
   P.rows_t &= ~1;  // keeps the bf16 block 16-byte aligned for any dv % 8 == 0
   if (P.rows_k < 1 || P.rows_m < 1 || P.rows_v < 1 || P.rows_t < 1) return false;
   P.tot_k = ns + w + m + H * m;
@@ -808,7 +807,7 @@ bool plan_step_tma(const DevState& s, void* plan_out) {
   P.mo_zhi = o;  o += H * m * 4;
   P.mo_zlo = o;  o += H * m * 4;
   P.misc_bytes = o;
-  if (o > kStageBytes) return false;
+  if (o > stage_bytes) return false;
   P.nrp = r4(ns + w);
   P.mp = r4(m);
   int x = 0;
@@ -835,19 +834,32 @@ bool plan_step_tma(const DevState& s, void* plan_out) {
   P.scratch_floats = x;
   P.ring_off = 1024;  // barriers and the abort flag live below
   // M stays resident through the per-head phase; the ring must hold it plus
-  // room for the producer to keep going.  Two CTAs per SM when the ring still
-  // has kMinRing2 stages in half the shared memory, else one.
-  for (int per_sm = 2; per_sm >= 1; --per_sm) {
-    const long budget = per_sm == 2 ? kSmemBudget2 : kSmemBudget;
-    const long avail = budget - P.ring_off - (long)x * 4;
-    int ring = (int)(avail / kStageBytes);
-    if (ring > kMaxRing) ring = kMaxRing;
-    if (ring < P.n_m + 2 || (per_sm == 2 && ring < kMinRing2)) continue;
-    P.ring = ring;
-    P.ctas_per_sm = per_sm;
-    P.smem_bytes = (size_t)P.ring_off + (size_t)ring * kStageBytes + (size_t)x * 4;
-    return true;
-  }
+  // room for the producer to keep going.
+  const long budget = per_sm == 2 ? kSmemBudget2 : kSmemBudget;
+  const long avail = budget - P.ring_off - (long)x * 4;
+  int ring = (int)(avail / stage_bytes);
+  if (ring > kMaxRing) ring = kMaxRing;
+  if (ring < P.n_m + 2 || ring < kMinRing) return false;
+  P.ring = ring;
+  P.ctas_per_sm = per_sm;
+  P.smem_bytes = (size_t)P.ring_off + (size_t)ring * stage_bytes + (size_t)x * 4;
+  return true;
+}
+
+// Plan the stage layout; false when the geometry is outside this kernel
+// (every bulk copy must start and end on 16 bytes, d and dv <= 128, H <= 8,
+// and the misc stage and the scratch must fit).  Preference, measured on the
+// 14336-group workload: two CTAs per SM (two groups in flight per SM) matter
+// most, then large stages (fewer hand-offs per group): 32 KB stages 0.707 ms,
+// 16 KB 0.774 ms; one CTA per SM 1.1-1.2 ms.
+bool plan_step_tma(const DevState& s, void* plan_out) {
+  TmaPlan& P = *static_cast<TmaPlan*>(plan_out);
+  const int d = s.d, dv = s.dv, m = s.m, H = s.heads;
+  if (H > 8 || d > 128 || dv > 128 || (dv & 7) || (d & 3) || ((H * m) & 3) || (m & 3))
+    return false;
+  const int tries[4][2] = {{32768, 2}, {16384, 2}, {32768, 1}, {16384, 1}};
+  for (const auto& t : tries)
+    if (plan_with(s, t[0], t[1], P)) return true;
   return false;
 }
 
