@@ -520,100 +520,91 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     }
     if (!csync()) { fail(g); return; }
 
-    // ---- B: per-head scalars with M from its stages.
-    const int ci_m = ci;
-    {
-      int i2 = ci;
-      uint32_t p2 = cpar;
-      for (int i = 0; i < P.n_m; ++i) {
-        if (!acquire_slot(i2, p2)) { fail(g); return; }
-        if (++i2 == S) {
-          i2 = 0;
-          p2 ^= 1u;
-        }
-      }
-    }
-    for (int hh = warp; hh < H; hh += kCWarps) {
-      const int64_t hb = g * H + hh;
-      float* hfh = fh + hh * P.mp;
-      float* hgs = gs + hh * P.mp;
-      float* hzs = zs + hh * P.mp;
-      float* hms = ms + hh * P.mp;
-      float* hsig = sig + hh * P.nrp;
-      for (int i = lane; i < m_eff; i += 32) {
-        const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
-        float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
-        if (full) {
-          const float l = lg[hh * P.mp + i];
-          if (l > mo) {
-            r = expf(mo - l);
-            mn = l;
+    // ---- B: per-head scalars.  M streams through the ring a stage at a time
+    // (each stage holds the blocks of heads_per_stage consecutive heads); a
+    // head's warp works as soon as its block has landed and every stage is
+    // handed back right after, so the ring never has to hold all of M.
+    const int heads_per_stage = P.rows_m / m;
+    for (int mst = 0; mst < P.n_m; ++mst, advance()) {
+      if (!acquire_slot(ci, cpar)) { fail(g); return; }
+      const int h_lo = mst * heads_per_stage;
+      const int h_hi = min(H, h_lo + heads_per_stage);
+      for (int hh = warp; hh < H; hh += kCWarps) {
+        if (hh < h_lo || hh >= h_hi) continue;
+        const int64_t hb = g * H + hh;
+        float* hfh = fh + hh * P.mp;
+        float* hgs = gs + hh * P.mp;
+        float* hzs = zs + hh * P.mp;
+        float* hms = ms + hh * P.mp;
+        float* hsig = sig + hh * P.nrp;
+        for (int i = lane; i < m_eff; i += 32) {
+          const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
+          float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
+          if (full) {
+            const float l = lg[hh * P.mp + i];
+            if (l > mo) {
+              r = expf(mo - l);
+              mn = l;
+            }
+            e = expf(l - mn);
+            comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
+            s.m_max[hb * m + i] = mn;
+            s.z_hat[hb * m + i] = zn;
+            s.z_lo[hb * m + i] = zln;
           }
-          e = expf(l - mn);
-          comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
-          s.m_max[hb * m + i] = mn;
-          s.z_hat[hb * m + i] = zn;
-          s.z_lo[hb * m + i] = zln;
+          rs[hh * P.mp + i] = r;
+          es[hh * P.mp + i] = e;
+          hzs[i] = zn + zln;
+          hms[i] = mn;
         }
-        rs[hh * P.mp + i] = r;
-        es[hh * P.mp + i] = e;
-        hzs[i] = zn + zln;
-        hms[i] = mn;
-      }
-      const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
-      if (full && lane == 0) s.far_len[hb] = fl_new;
-      __syncwarp();
-      float cmax = -INFINITY;
-      for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
-      cmax = warp_max(cmax);
-      float c_all = cmax, far_den = 0.f;
-      if (fl_new > 0) {
-        float f = -INFINITY;
-        for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
-        f = warp_max(f);
-        for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
+        const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
+        if (full && lane == 0) s.far_len[hb] = fl_new;
         __syncwarp();
-        // This head's m x m block of M sits inside one stage (rows_m % m == 0).
-        int mrow0 = hh * m, mslot = ci_m;
-        while (mrow0 >= P.rows_m) {  // at most n_m - 1 steps
-          mrow0 -= P.rows_m;
-          if (++mslot == S) mslot = 0;
-        }
-        const float* Mh = reinterpret_cast<const float*>(stage_ptr(mslot)) + (size_t)mrow0 * m;
-        float cm = -INFINITY;
-        for (int b = lane; b < m_eff; b += 32) {
-          float u = dot2(hfh, Mh + b, m, m_eff);
-          if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
-          hgs[b] = u;
-          cm = fmaxf(cm, f + hms[b]);
-        }
-        c_all = fmaxf(cmax, warp_max(cm));
-        float acc = 0.f;
-        for (int b = lane; b < m_eff; b += 32) {
-          const float gb = hgs[b] * expf(f + hms[b] - c_all);
-          hgs[b] = gb;
-          acc = fmaf(gb, hzs[b], acc);
-        }
-        far_den = warp_sum(acc);
-        if (!(far_den >= 0.f)) {
-          far_den = 0.f;
+        float cmax = -INFINITY;
+        for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
+        cmax = warp_max(cmax);
+        float c_all = cmax, far_den = 0.f;
+        if (fl_new > 0) {
+          float f = -INFINITY;
+          for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
+          f = warp_max(f);
+          for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
+          __syncwarp();
+          // This head's m x m block of M, inside the current M stage.
+          const float* Mh = reinterpret_cast<const float*>(stage_ptr(ci)) +
+                            (size_t)(hh - h_lo) * m * m;
+          float cm = -INFINITY;
+          for (int b = lane; b < m_eff; b += 32) {
+            float u = dot2(hfh, Mh + b, m, m_eff);
+            if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
+            hgs[b] = u;
+            cm = fmaxf(cm, f + hms[b]);
+          }
+          c_all = fmaxf(cmax, warp_max(cm));
+          float acc = 0.f;
+          for (int b = lane; b < m_eff; b += 32) {
+            const float gb = hgs[b] * expf(f + hms[b] - c_all);
+            hgs[b] = gb;
+            acc = fmaf(gb, hzs[b], acc);
+          }
+          far_den = warp_sum(acc);
+          if (!(far_den >= 0.f)) {
+            far_den = 0.f;
+            for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+          }
+        } else {
           for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
         }
-      } else {
-        for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+        float psum = 0.f;
+        for (int j = lane; j < nnear; j += 32) {
+          const float p = expf(hsig[j] - c_all);
+          hsig[j] = p;
+          psum += p;
+        }
+        psum = warp_sum(psum);
+        if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
       }
-      float psum = 0.f;
-      for (int j = lane; j < nnear; j += 32) {
-        const float p = expf(hsig[j] - c_all);
-        hsig[j] = p;
-        psum += p;
-      }
-      psum = warp_sum(psum);
-      if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
-    }
-    for (int i = 0; i < P.n_m; ++i) {
       release_slot(ci);
-      advance();
     }
     if (!csync()) { fail(g); return; }
 
@@ -833,13 +824,11 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.x_part = x; x += (kCWarps / 2) * ht * 128;
   P.scratch_floats = x;
   P.ring_off = 1024;  // barriers and the abort flag live below
-  // M stays resident through the per-head phase; the ring must hold it plus
-  // room for the producer to keep going.
   const long budget = per_sm == 2 ? kSmemBudget2 : kSmemBudget;
   const long avail = budget - P.ring_off - (long)x * 4;
   int ring = (int)(avail / stage_bytes);
   if (ring > kMaxRing) ring = kMaxRing;
-  if (ring < P.n_m + 2 || ring < kMinRing) return false;
+  if (ring < kMinRing) return false;
   P.ring = ring;
   P.ctas_per_sm = per_sm;
   P.smem_bytes = (size_t)P.ring_off + (size_t)ring * stage_bytes + (size_t)x * 4;
