@@ -7,8 +7,9 @@
 //     keys -- K~ = seg_means(k) (prefill_shared), sinks, ring fill, counters;
 //     block (g, 1 + h) takes head h's queries -- Q~_h = seg_means(q_h)
 //     (NystromHead::seal).  Segment i covers rows [i t / m_eff,
-//     (i+1) t / m_eff); sums are accumulated in f64 (fn seg_means).  The f64
-//     means go to a workspace for step 2, their f32 roundings to the state.
+//     (i+1) t / m_eff); sums keep f64 accuracy (fn seg_means accumulates in
+//     f64).  The f64 means go to a workspace for step 2, their f32 roundings
+//     to the state.
 //  2. pinv_kernel, one block per (group, head): A = exp(Q~64 K~64^T * scale)
 //     in f64, then M = (A^T A + lambda I)^-1 A^T (fn ridge_pinv):
 //     lambda = 1e-6 * max(mean diag(A^T A), DBL_MIN); a failed Cholesky
@@ -44,11 +45,40 @@ __device__ __forceinline__ void st4(float* p, float4 x) {
 }
 
 // ---------------------------------------------------------------- 1
+// Knuth's two-sum: a + b = s + e exactly in f32.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// Sum of 8 f32 values as hi + lo with hi = the f32 sum of a balanced tree and
+// lo = the exact rounding errors of its seven additions (accumulated in f32,
+// whose own rounding is ~2^-48 of the total).
+__device__ __forceinline__ void sum8(const float (&x)[8], float& hi, float& lo) {
+  float s01, e01, s23, e23, s45, e45, s67, e67, s03, e03, s47, e47;
+  two_sum(x[0], x[1], s01, e01);
+  two_sum(x[2], x[3], s23, e23);
+  two_sum(x[4], x[5], s45, e45);
+  two_sum(x[6], x[7], s67, e67);
+  two_sum(s01, s23, s03, e03);
+  two_sum(s45, s67, s47, e47);
+  float e;
+  two_sum(s03, s47, hi, e);
+  lo = ((e01 + e23) + (e45 + e67)) + ((e03 + e47) + e);
+}
+
+// One block per (group, row source): y = 0 reads the group's keys (K~ plus
+// sinks, ring and counters), y = 1 + h head h's queries (Q~_h).  One warp per
+// landmark segment, lanes over float4 columns: no cross-warp reduction.  Rows
+// are summed eight at a time exactly (sum8) and each such partial enters an
+// f64 accumulator with one f64 addition, so the segment sums keep f64
+// accuracy (within ~1e-14 of a sequential f64 sum) at an eighth of the f64
+// additions -- GB300's f64 rate, not HBM, bounds a plain f64 loop here.
 __global__ void __launch_bounds__(kThreads)
 landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
                  const float* __restrict__ q, const float* __restrict__ k,
                  const float* __restrict__ v, double* __restrict__ ws) {
-  __shared__ double red[kWarps][128];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t gi = blockIdx.x, g = g0 + gi;
   const int r = blockIdx.y;  // 0: keys, 1 + h: queries of head h
@@ -69,38 +99,55 @@ landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
   }
   double* dst64 = ws + (gi * (1 + H) + r) * (int64_t)m * d;
 
-  for (int i = 0; i < m_eff; ++i) {
+  for (int i = warp; i < m_eff; i += kWarps) {
     const int lo = (int)(((int64_t)i * t) / m_eff);
     const int hi = (int)(((int64_t)(i + 1) * t) / m_eff);
     const double inv = 1.0 / (double)(hi - lo);
-    for (int ct = 0; ct < d; ct += 128) {
-      const int c4 = (ct >> 2) + lane;
-      const bool cv = c4 < d4;
+    for (int c4 = lane; c4 < d4; c4 += 32) {
+      const float* col = src + 4 * c4;
       double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
-      if (cv) {
-#pragma unroll 4
-        for (int j = lo + warp; j < hi; j += kWarps) {
-          const float4 x = ld4(src + (int64_t)j * d + 4 * c4);
-          a0 += (double)x.x;
-          a1 += (double)x.y;
-          a2 += (double)x.z;
-          a3 += (double)x.w;
-        }
-        red[warp][4 * lane + 0] = a0;
-        red[warp][4 * lane + 1] = a1;
-        red[warp][4 * lane + 2] = a2;
-        red[warp][4 * lane + 3] = a3;
-      }
-      __syncthreads();
-      if (tid < 128 && ct + tid < d) {
-        double sum = 0.0;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      int j = lo;
+      for (; j + 8 <= hi; j += 8) {
+        float x0[8], x1[8], x2[8], x3[8];
 #pragma unroll
-        for (int wp = 0; wp < kWarps; ++wp) sum += red[wp][tid];
-        const double mean = sum * inv;
-        dst64[(int64_t)i * d + ct + tid] = mean;
-        dst32[(int64_t)i * d + ct + tid] = (float)mean;
+        for (int u = 0; u < 8; ++u) {
+          const float4 x = ld4(col + (int64_t)(j + u) * d);
+          x0[u] = x.x;
+          x1[u] = x.y;
+          x2[u] = x.z;
+          x3[u] = x.w;
+        }
+        float h, e;
+        sum8(x0, h, e);
+        a0 += (double)h;
+        l0 += e;
+        sum8(x1, h, e);
+        a1 += (double)h;
+        l1 += e;
+        sum8(x2, h, e);
+        a2 += (double)h;
+        l2 += e;
+        sum8(x3, h, e);
+        a3 += (double)h;
+        l3 += e;
       }
-      __syncthreads();
+      for (; j < hi; ++j) {
+        const float4 x = ld4(col + (int64_t)j * d);
+        a0 += (double)x.x;
+        a1 += (double)x.y;
+        a2 += (double)x.z;
+        a3 += (double)x.w;
+      }
+      const double m0 = (a0 + (double)l0) * inv, m1 = (a1 + (double)l1) * inv;
+      const double m2 = (a2 + (double)l2) * inv, m3 = (a3 + (double)l3) * inv;
+      double* o64 = dst64 + (int64_t)i * d + 4 * c4;
+      o64[0] = m0;
+      o64[1] = m1;
+      o64[2] = m2;
+      o64[3] = m3;
+      float* o32 = dst32 + (int64_t)i * d + 4 * c4;
+      st4(o32, make_float4((float)m0, (float)m1, (float)m2, (float)m3));
     }
   }
 
