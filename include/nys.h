@@ -140,6 +140,9 @@ typedef struct {
   int32_t t;        /* prompt length the group was sealed with                */
   int32_t win_len;  /* keys in the window (w once sealed)                     */
   int32_t win_head; /* ring slot of the oldest window key                     */
+  int32_t status;   /* 0, or nonzero when a decode launch's bounded wait gave
+                       up before this group was stepped (its state is stale
+                       and its last outputs are not valid)                    */
 } nys_group_info;
 
 /* Bytes of device memory a handle of n_groups groups needs (nystrom.rs,
@@ -268,6 +271,15 @@ int nys_layout_of(const nys_states* st, void** base, nys_layout* layout);
  * ring full).  Host bookkeeping only; nothing is launched.
  * Errors: NYS_E_INVAL, NYS_E_RANGE. */
 int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n);
+
+/* Test hook, no counterpart on the pages: the next nys_step_batch on this
+ * handle makes its first CTA withhold ring stage `stage` (counted from 0 over
+ * that CTA's groups), so that CTA's bounded waits run out after 2 s and it
+ * marks its groups' status words.  Exercises the decode kernel's timeout path
+ * without faulting or hanging the GPU; the context stays usable and re-sealing
+ * clears the status.  Only the fast decode kernel (d, dv <= 128, heads <= 8)
+ * waits on anything.  Errors: NYS_E_INVAL. */
+int nys_debug_stall_once(nys_states* st, int32_t stage);
 
 /* The geometry a handle was created with.  Errors: NYS_E_INVAL. */
 int nys_config_of(const nys_states* st, nys_config* cfg, int64_t* n_groups);

@@ -21,6 +21,7 @@ struct nys_states {
   std::vector<uint8_t> sealed;  // host record of groups with a sealed state
   std::vector<int32_t> exact_len;  // keys held by exact-only groups, -1 otherwise
   int64_t n_exact;                 // how many groups are exact-only
+  int debug_skip;                  // test hook for the next decode launch
   int device;
 };
 
@@ -246,6 +247,7 @@ int nys_alloc_states(const nys_config* cfg, int64_t n_groups, void* dev_buf,
   st->sealed.assign((size_t)n_groups, 0);
   st->exact_len.assign((size_t)n_groups, -1);
   st->n_exact = 0;
+  st->debug_skip = -1;
   *out = st;
   return NYS_OK;
 }
@@ -407,7 +409,9 @@ int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
   }
   const nys::DevState ds = dev_state(st);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (exact_here < n && nys::launch_step(ds, g0, n, q, k, v, out, s) != cudaSuccess)
+  const int skip = st->debug_skip;
+  st->debug_skip = -1;
+  if (exact_here < n && nys::launch_step(ds, g0, n, q, k, v, out, s, skip) != cudaSuccess)
     return NYS_E_CUDA;
   if (exact_here) {
     if (nys::launch_exact_step(ds, g0, n, q, k, v, out, s) != cudaSuccess) return NYS_E_CUDA;
@@ -437,6 +441,7 @@ int nys_query(const nys_states* st, int64_t g, nys_group_info* info, int32_t* fa
   info->m_eff = ints[nys::kIntMEff];
   info->t = ints[nys::kIntT];
   info->mode = ints[nys::kIntMode];
+  info->status = ints[nys::kIntStatus];
   return NYS_OK;
 }
 
@@ -453,6 +458,12 @@ int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n) {
   if (rc) return rc;
   if (n) std::memset(st->sealed.data() + g0, 1, (size_t)n);
   forget_exact(st, g0, n);
+  return NYS_OK;
+}
+
+int nys_debug_stall_once(nys_states* st, int32_t stage) {
+  if (!st || stage < 0) return NYS_E_INVAL;
+  st->debug_skip = stage;
   return NYS_OK;
 }
 

@@ -148,9 +148,11 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 #endif
 
 // One decode token for groups [g0, g0+n): one kernel launch on `stream`.
+// debug_skip >= 0 (test hook) makes the fast kernel's first CTA withhold that
+// ring stage, so its bounded waits run out.
 cudaError_t launch_step(const DevState& s, int64_t g0, int64_t n,
                         const float* q, const float* k, const float* v,
-                        float* out, cudaStream_t stream);
+                        float* out, cudaStream_t stream, int debug_skip = -1);
 
 // Fast path of the step (nys_step_tma.cu): plan_step_tma fills an opaque
 // plan of at most kPlanBytes and returns false for geometries it does not
@@ -160,7 +162,7 @@ bool plan_step_tma(const DevState& s, void* plan_out);
 size_t step_tma_plan_bytes();
 cudaError_t launch_step_tma(const DevState& s, const void* plan, int64_t g0, int64_t n,
                             const float* q, const float* k, const float* v, float* out,
-                            cudaStream_t stream);
+                            cudaStream_t stream, int debug_skip = -1);
 
 // Prompt geometry of a seal launch.  Uniform batches (every group has prompt
 // length t and m_eff landmarks, group i's rows start at i * t) leave the

@@ -181,6 +181,7 @@ landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
     ints[kIntMEff] = m_eff;
     ints[kIntT] = t;
     ints[kIntMode] = kModeSealed;
+    ints[kIntStatus] = 0;
   }
   for (int h = tid; h < H; h += kThreads) s.far_len[g * H + h] = t - ns - w;
 }

@@ -393,13 +393,13 @@ cudaError_t launch_tile(const DevState& s, int64_t g0, int64_t n,
 
 cudaError_t launch_step(const DevState& s, int64_t g0, int64_t n,
                         const float* q, const float* k, const float* v,
-                        float* out, cudaStream_t stream) {
+                        float* out, cudaStream_t stream, int debug_skip) {
   if (n <= 0) return cudaSuccess;
   // Geometries the persistent TMA kernel covers take it; the rest (H > 8,
   // dv > 128, rows that are not 16-byte multiples) run the kernel below.
   alignas(16) unsigned char plan[kPlanBytes];
   if (step_tma_plan_bytes() <= sizeof(plan) && plan_step_tma(s, plan))
-    return launch_step_tma(s, plan, g0, n, q, k, v, out, stream);
+    return launch_step_tma(s, plan, g0, n, q, k, v, out, stream, debug_skip);
   if (s.heads == 1) return launch_tile<1>(s, g0, n, q, k, v, out, stream);
   if (s.heads == 2) return launch_tile<2>(s, g0, n, q, k, v, out, stream);
   if (s.heads <= 4) return launch_tile<4>(s, g0, n, q, k, v, out, stream);

@@ -57,6 +57,7 @@ struct TmaPlan {
   int x_sig, x_fh, x_lg, x_rs, x_es, x_gs, x_zs, x_ms, x_den, x_fl, x_ints, x_part;
   int nrp, mp, scratch_floats;
   int ring;
+  int debug_skip;   // test hook: ring stage CTA 0 withholds (-1: none)
   int stage_bytes;  // 32 KB when the ring still fits, else 16 KB
   int ctas_per_sm;
   int ring_off;  // bytes from the smem base to the ring
@@ -207,6 +208,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     int idx = 0;           // c % S
     uint32_t phase = 0;    // (c / S) & 1
     bool ok = true;
+    int64_t gfail = n;     // first group left unstepped, when a wait gave up
     // The ring slot of the next group is read one group ahead so that the
     // load's latency overlaps the current group's copies.
     int3 nxt = make_int3(0, 0, 0);
@@ -230,10 +232,12 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
            ++st, ++c, idx = (idx + 1 == S) ? 0 : idx + 1, phase ^= (idx == 0) ? 1u : 0u) {
         if (!wait_bar(&empty[idx], phase ^ 1u, abort)) {
           ok = false;
+          gfail = gi;
           break;
         }
         unsigned char* dst = ring + (size_t)idx * P.stage_bytes;
         uint64_t* bar = &full[idx];
+        if ((int)c == P.debug_skip && blockIdx.x == 0) continue;  // test hook
         if (st == 0) {
           mbar_expect_tx(bar, (uint32_t)P.misc_bytes);
           bulk_load(dst + P.mo_ints, ints, kIntsPerGroup * 4, bar);
@@ -292,12 +296,15 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     }
     if (!ok) {
       atomicExch(abort, 1);
-      if (blockIdx.x < n) s.ints[(g0 + blockIdx.x) * kIntsPerGroup + kIntStatus] = 1;
+      for (int64_t g2 = g0 + gfail; g2 < g0 + n; g2 += gridDim.x)
+        s.ints[g2 * kIntsPerGroup + kIntStatus] = 1;
     }
     // Whatever happened, no copy may still be landing in shared memory when
     // the CTA exits: wait (bounded) for the last S stages issued.
     const uint32_t first = c > (uint32_t)S ? c - (uint32_t)S : 0u;
-    for (uint32_t cc = first; cc < c; ++cc) wait_bar(&full[cc % S], (cc / S) & 1u, nullptr);
+    for (uint32_t cc = first; cc < c; ++cc)
+      if (!((int)cc == P.debug_skip && blockIdx.x == 0))
+        wait_bar(&full[cc % S], (cc / S) & 1u, nullptr);
     return;  // (the division above runs once, at exit)
   }
 
@@ -351,7 +358,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   };
   auto fail = [&](int64_t g) {
     atomicExch(abort, 1);
-    s.ints[g * kIntsPerGroup + kIntStatus] = 1;
+    // this group and every later one of this CTA are left unstepped
+    if (lane == 0)
+      for (int64_t g2 = g; g2 < g0 + n; g2 += gridDim.x)
+        s.ints[g2 * kIntsPerGroup + kIntStatus] = 1;
   };
 
   for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x) {
@@ -830,6 +840,7 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   if (ring > kMaxRing) ring = kMaxRing;
   if (ring < kMinRing) return false;
   P.ring = ring;
+  P.debug_skip = -1;
   P.ctas_per_sm = per_sm;
   P.smem_bytes = (size_t)P.ring_off + (size_t)ring * stage_bytes + (size_t)x * 4;
   return true;
@@ -856,8 +867,9 @@ size_t step_tma_plan_bytes() { return sizeof(TmaPlan); }
 
 cudaError_t launch_step_tma(const DevState& s, const void* plan, int64_t g0, int64_t n,
                             const float* q, const float* k, const float* v, float* out,
-                            cudaStream_t stream) {
-  const TmaPlan& P = *static_cast<const TmaPlan*>(plan);
+                            cudaStream_t stream, int debug_skip) {
+  TmaPlan P = *static_cast<const TmaPlan*>(plan);
+  P.debug_skip = debug_skip;
   if (n <= 0) return cudaSuccess;
   if (s.heads == 1) return launch_tma_ht<1>(s, P, g0, n, q, k, v, out, stream);
   if (s.heads == 2) return launch_tma_ht<2>(s, P, g0, n, q, k, v, out, stream);

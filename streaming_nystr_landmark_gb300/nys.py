@@ -35,7 +35,7 @@ EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
             "nys_mark_sealed", "nys_config_of", "nys_strerror",
             "nys_seal_static", "nys_seal_ragged", "nys_o1_begin", "nys_o1_push_q",
             "nys_o1_seal", "nys_o1_sealed", "nys_o1_step", "nys_o1_memory_bytes",
-            "nys_o1_states", "nys_o1_free")
+            "nys_o1_states", "nys_o1_free", "nys_debug_stall_once")
 
 
 class NysConfig(ctypes.Structure):
@@ -61,7 +61,7 @@ class NysLayout(ctypes.Structure):
 class NysGroupInfo(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("m_eff", ctypes.c_int32),
                 ("t", ctypes.c_int32), ("win_len", ctypes.c_int32),
-                ("win_head", ctypes.c_int32)]
+                ("win_head", ctypes.c_int32), ("status", ctypes.c_int32)]
 
 
 def _load():
@@ -92,6 +92,7 @@ def _load():
         "nys_o1_memory_bytes": [VP, P(ctypes.c_size_t)],
         "nys_o1_states": [VP, P(VP)],
         "nys_o1_free": [VP],
+        "nys_debug_stall_once": [VP, I32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -173,7 +174,12 @@ def nys_query(handle, g, heads, stream=0):
     _check(_lib.nys_query(handle, g, ctypes.byref(info), far, stream or None),
            "nys_query")
     return ({"mode": info.mode, "m_eff": info.m_eff, "t": info.t,
-             "win_len": info.win_len, "win_head": info.win_head}, list(far))
+             "win_len": info.win_len, "win_head": info.win_head,
+             "status": info.status}, list(far))
+
+
+def nys_debug_stall_once(handle, stage):
+    _check(_lib.nys_debug_stall_once(handle, stage), "nys_debug_stall_once")
 
 
 def nys_layout_of(handle):
@@ -288,6 +294,11 @@ class NystromStates:
 
     def query(self, g):
         return nys_query(self.handle, g, self.cfg.heads_per_kv, self._stream())
+
+    def debug_stall_once(self, stage):
+        """Test hook: the next step's first CTA withholds ring stage `stage`,
+        so its bounded waits run out and its groups report status 1."""
+        nys_debug_stall_once(self.handle, stage)
 
     def region(self, name):
         """A torch view of one state region, shaped as nys_layout documents."""

@@ -59,7 +59,7 @@ def test_error_codes_on_device(cuda_device):
     torch.cuda.synchronize()
     info, far = st.query(3)
     assert info == {"mode": 1, "m_eff": 8, "t": 64, "win_len": 16,
-                    "win_head": (64 - 4 + 1) % 16}
+                    "win_head": (64 - 4 + 1) % 16, "status": 0}
     assert far == [64 - 4 - 16 + 1] * 2
     st.close()
 
