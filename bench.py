@@ -558,6 +558,9 @@ def main():
     ap.add_argument("--groups", type=int, default=0,
                     help="override the workload's group count (profiling on a "
                          "smaller case); 0 keeps the workload's own")
+    ap.add_argument("--prompt", type=int, default=0,
+                    help="override the workload's prompt length (profiling the "
+                         "decode step without the full prompt); 0 keeps it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -566,6 +569,8 @@ def main():
     if args.groups:
         wl = wl.with_(name=f"{wl.name}[{args.groups} groups]", seqs=1, layers=1,
                       kv_groups=args.groups)
+    if args.prompt:
+        wl = wl.with_(name=f"{wl.name}[prompt {args.prompt}]", t=args.prompt)
     if args.impl == "reference":
         run_reference(args, wl)
     elif args.mode == "seal":

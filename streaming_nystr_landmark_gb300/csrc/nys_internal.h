@@ -94,6 +94,19 @@ __device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, 
   nlo = t - (nhi - s);
 }
 
+// comp_axpy with r == 1, for callers that branch on r once for many elements.
+__device__ __forceinline__ void comp_add(float hi, float lo, float x, float y, float& nhi,
+                                         float& nlo) {
+  const float b = x * y;
+  const float pb = fmaf(x, y, -b);
+  const float s = hi + b;
+  const float sb = s - hi;
+  const float es = (hi - (s - sb)) + (b - sb);
+  const float t = lo + (pb + es);
+  nhi = s + t;
+  nlo = t - (nhi - s);
+}
+
 // Compensated dot product (Ogita, Rump and Oishi's Dot2): sum_a x[a] * y[a*ys]
 // with each product's rounding error recovered by FMA and each addition's by
 // two-sum, so the result is as accurate as if accumulated in twice the

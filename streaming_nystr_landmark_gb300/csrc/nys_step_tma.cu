@@ -36,6 +36,7 @@ constexpr int kCThreads = kCWarps * 32;
 constexpr int kThreadsTma = kCThreads + 32;
 constexpr int kMaxRing = 12;
 constexpr int kRowsPerRound = 4;
+constexpr int kQRows = 8;  // Q~ rows a warp reduces at once (generic path)
 constexpr uint64_t kWaitNs = 2000000000ull;  // every wait gives up after 2 s
 constexpr uint32_t kSuspendNs = 1000000;      // a waiting thread sleeps up to 1 ms per try
 constexpr int kSmemBudget = 227 * 1024;    // one CTA per SM
@@ -113,6 +114,28 @@ __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
+}
+// Three (two) independent warp reductions interleaved: the same trees as
+// warp_max / warp_sum, one latency chain instead of several.
+__device__ __forceinline__ void warp_max3(float& a, float& b, float& c) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, a, o);
+    const float y = __shfl_xor_sync(0xffffffffu, b, o);
+    const float z = __shfl_xor_sync(0xffffffffu, c, o);
+    a = fmaxf(a, x);
+    b = fmaxf(b, y);
+    c = fmaxf(c, z);
+  }
+}
+__device__ __forceinline__ void warp_sum2(float& a, float& b) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, a, o);
+    const float y = __shfl_xor_sync(0xffffffffu, b, o);
+    a += x;
+    b += y;
+  }
 }
 
 // Sum each of V per-lane partials over the 32 lanes.  Returns, in every lane,
@@ -479,26 +502,22 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           }
         }
       } else {
-      for (int base = 0; base < nrow; base += kCWarps * kRowsPerRound) {
+      // Rows before kend are keys (dotted with every head's query); the rest
+      // are Q~ rows, each dotted with the evicted key only.
+      const int kend = min(nrow, max(0, ns + w + m - r0));
+      for (int base = 0; base < kend; base += kCWarps * kRowsPerRound) {
         float x[kRowsPerRound * HT];
 #pragma unroll
         for (int i = 0; i < kRowsPerRound * HT; ++i) x[i] = 0.f;
 #pragma unroll
         for (int u = 0; u < kRowsPerRound; ++u) {
           const int lr = base + warp * kRowsPerRound + u;
-          if (lr < nrow) {
+          if (lr < kend && ck) {
             const int vr = r0 + lr;
-            const float* row = stage + (size_t)lr * d;
-            if (vr < ns + w + m) {
-              if (vr - ns == slot) row = xknew;
-              if (ck) {
-                const float4 a = ld4(row + 4 * lane);
+            const float* row = (vr - ns == slot && vr >= ns) ? xknew : stage + (size_t)lr * d;
+            const float4 a = ld4(row + 4 * lane);
 #pragma unroll
-                for (int hh = 0; hh < HT; ++hh) x[u * HT + hh] = dot4(a, qr[hh]);
-              }
-            } else if (ck) {
-              x[u * HT] = dot4(ld4(row + 4 * lane), kev4);
-            }
+            for (int hh = 0; hh < HT; ++hh) x[u * HT + hh] = dot4(a, qr[hh]);
           }
         }
         const float tot = reduce_multi<kRowsPerRound * HT>(x, lane);
@@ -506,22 +525,33 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           const int vi = reduce_index<kRowsPerRound * HT>(lane);
           const int u = vi / HT, hh = vi - u * HT;
           const int lr = base + warp * kRowsPerRound + u;
-          if (lr < nrow) {
+          if (lr < kend && hh < H) {
             const int vr = r0 + lr;
             const float l = tot * scale;
-            if (vr < ns + w) {
-              if (hh < H) sig[hh * P.nrp + vr] = l;
-            } else if (vr < ns + w + m) {
-              if (hh < H) fh[hh * P.mp + (vr - ns - w)] = l;
-            } else if (hh == 0) {
-              int qr = vr - ns - w - m;
-              int h = 0;
-              while (qr >= m) {  // at most H - 1 steps
-                qr -= m;
-                ++h;
-              }
-              lg[h * P.mp + qr] = l;
+            if (vr < ns + w) sig[hh * P.nrp + vr] = l;
+            else fh[hh * P.mp + (vr - ns - w)] = l;
+          }
+        }
+      }
+      // Q~ rows, kQRows per warp: one value per row, reduced all at once.
+      for (int base = kend + warp * kQRows; base < nrow; base += kCWarps * kQRows) {
+        float x[kQRows];
+#pragma unroll
+        for (int u = 0; u < kQRows; ++u) {
+          const int lr = base + u;
+          x[u] = (lr < nrow && ck) ? dot4(ld4(stage + (size_t)lr * d + 4 * lane), kev4) : 0.f;
+        }
+        const float tot = reduce_multi<kQRows>(x, lane);
+        if (reduce_writer<kQRows>(lane)) {
+          const int lr = base + reduce_index<kQRows>(lane);
+          if (lr < nrow) {
+            int qr = r0 + lr - (ns + w + m);
+            int h = 0;
+            while (qr >= m) {  // at most H - 1 steps
+              qr -= m;
+              ++h;
             }
+            lg[h * P.mp + qr] = tot * scale;
           }
         }
       }
@@ -547,6 +577,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         float* hzs = zs + hh * P.mp;
         float* hms = ms + hh * P.mp;
         float* hsig = sig + hh * P.nrp;
+        // (1) Landmark updates: delayed insertion of the evicted key with
+        //     the running-maximum rescale.  mx_m collects the maximum of the
+        //     new running maxima.
+        float mx_m = -INFINITY;
         for (int i = lane; i < m_eff; i += 32) {
           const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
           float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
@@ -566,52 +600,54 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           es[hh * P.mp + i] = e;
           hzs[i] = zn + zln;
           hms[i] = mn;
+          mx_m = fmaxf(mx_m, mn);
         }
         const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
         if (full && lane == 0) s.far_len[hb] = fl_new;
-        __syncwarp();
-        float cmax = -INFINITY;
+        const bool has_far = fl_new > 0;
+        // (2) The maxima: near logits, landmark logits f, and the running
+        //     maxima, reduced together.  max_b (f + m_b) = f + max_b m_b
+        //     exactly, since rounding is monotonic.
+        float cmax = -INFINITY, f = -INFINITY;
         for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
-        cmax = warp_max(cmax);
-        float c_all = cmax, far_den = 0.f;
-        if (fl_new > 0) {
-          float f = -INFINITY;
+        if (has_far)
           for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
-          f = warp_max(f);
+        warp_max3(cmax, f, mx_m);
+        const float c_all = has_far ? fmaxf(cmax, f + mx_m) : cmax;
+        if (has_far)
           for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
-          __syncwarp();
-          // This head's m x m block of M, inside the current M stage.
-          const float* Mh = reinterpret_cast<const float*>(stage_ptr(ci)) +
-                            (size_t)(hh - h_lo) * m * m;
-          float cm = -INFINITY;
-          for (int b = lane; b < m_eff; b += 32) {
-            float u = dot2(hfh, Mh + b, m, m_eff);
-            if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
-            hgs[b] = u;
-            cm = fmaxf(cm, f + hms[b]);
-          }
-          c_all = fmaxf(cmax, warp_max(cm));
-          float acc = 0.f;
-          for (int b = lane; b < m_eff; b += 32) {
-            const float gb = hgs[b] * expf(f + hms[b] - c_all);
-            hgs[b] = gb;
-            acc = fmaf(gb, hzs[b], acc);
-          }
-          far_den = warp_sum(acc);
-          if (!(far_den >= 0.f)) {
-            far_den = 0.f;
-            for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
-          }
-        } else {
-          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
-        }
+        // (3) Near weights on the joint scale.
         float psum = 0.f;
         for (int j = lane; j < nnear; j += 32) {
           const float p = expf(hsig[j] - c_all);
           hsig[j] = p;
           psum += p;
         }
-        psum = warp_sum(psum);
+        // (4) Far mix u = F^ M (rectified), weights g_b on the joint scale,
+        //     far denominator; both sums reduced together.
+        float acc = 0.f;
+        if (has_far) {
+          __syncwarp();
+          // This head's m x m block of M, inside the current M stage.
+          const float* Mh = reinterpret_cast<const float*>(stage_ptr(ci)) +
+                            (size_t)(hh - h_lo) * m * m;
+          for (int b = lane; b < m_eff; b += 32) {
+            float u = dot2(hfh, Mh + b, m, m_eff);
+            if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
+            const float gb = u * expf(f + hms[b] - c_all);
+            hgs[b] = gb;
+            acc = fmaf(gb, hzs[b], acc);
+          }
+        } else {
+          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+        }
+        warp_sum2(acc, psum);
+        float far_den = has_far ? acc : 0.f;
+        // Guard: a negative (or NaN) far denominator drops the far field.
+        if (has_far && !(far_den >= 0.f)) {
+          far_den = 0.f;
+          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+        }
         if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
       }
       release_slot(ci);
@@ -649,6 +685,25 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     // (head, landmark) of T^ rows, stepped without dividing by m: (sh, sb) is
     // the current stage's first row, (th, tb) this warp's next row.
     int sh = 0, sb = 0;
+    // Many heads: a warp's rows come head by head, so their far numerator
+    // collects in one accumulator that is added to its head's once the head
+    // changes (with one or two heads a predicated add per row is cheaper).
+    float4 tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int hcur = 0;
+    auto flush_far = [&]() {
+#pragma unroll
+      for (int hh = 0; hh < HT; ++hh) {
+        if (hh == hcur) {
+          acc[hh].x += tacc.x;
+          acc[hh].y += tacc.y;
+          acc[hh].z += tacc.z;
+          acc[hh].w += tacc.w;
+        }
+      }
+      tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float* const t_hi_g = s.t_hat + (g * H * (int64_t)m) * dv + 4 * lane;
+    uint16_t* const t_lo_g = s.t_lo + (g * H * (int64_t)m) * dv + 4 * lane;
     for (int st = 0; st < P.n_t; ++st, advance()) {
       if (!acquire_slot(ci, cpar)) { fail(g); return; }
       const unsigned char* stage = stage_ptr(ci);
@@ -674,37 +729,74 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           tb -= m;
           ++th;
         }
+        if constexpr (HT > 2) {
+          if (h != hcur) {  // warp-uniform
+            flush_far();
+            hcur = h;
+          }
+        }
         if (b < m_eff && cv) {
           float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
           const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
           float4 lo = make_float4(bf16_lo(lr2.x), bf16_hi(lr2.x), bf16_lo(lr2.y), bf16_hi(lr2.y));
-          const int64_t grow = (g * H + h) * (int64_t)m + b;
           if (full) {
             const float r = rs[h * P.mp + b], e = es[h * P.mp + b];
-            comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
-            comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
-            comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
-            comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
-            st4(s.t_hat + grow * dv + 4 * lane, x);
+            float* thp;
+            uint16_t* tlp;
+            if constexpr (HT > 2) {
+              // Many heads: the compensated update branches once per row on
+              // r (no new running maximum is the common case).
+              if (r == 1.f) {
+                comp_add(x.x, lo.x, e, ve.x, x.x, lo.x);
+                comp_add(x.y, lo.y, e, ve.y, x.y, lo.y);
+                comp_add(x.z, lo.z, e, ve.z, x.z, lo.z);
+                comp_add(x.w, lo.w, e, ve.w, x.w, lo.w);
+              } else {
+                comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
+                comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
+                comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
+                comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
+              }
+              const int row = r0 + lr;  // = h * m + b
+              thp = t_hi_g + (size_t)row * dv;
+              tlp = t_lo_g + (size_t)row * dv;
+            } else {
+              comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
+              comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
+              comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
+              comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
+              const int64_t grow = (g * H + h) * (int64_t)m + b;
+              thp = s.t_hat + grow * dv + 4 * lane;
+              tlp = s.t_lo + grow * dv + 4 * lane;
+            }
+            st4(thp, x);
             uint2 lw;
             lw.x = pack_bf16x2(lo.x, lo.y);
             lw.y = pack_bf16x2(lo.z, lo.w);
-            *reinterpret_cast<uint2*>(s.t_lo + grow * dv + 4 * lane) = lw;
+            *reinterpret_cast<uint2*>(tlp) = lw;
           }
           const float gb = gs[h * P.mp + b];
+          if constexpr (HT > 2) {
+            tacc.x = fmaf(gb, x.x + lo.x, tacc.x);
+            tacc.y = fmaf(gb, x.y + lo.y, tacc.y);
+            tacc.z = fmaf(gb, x.z + lo.z, tacc.z);
+            tacc.w = fmaf(gb, x.w + lo.w, tacc.w);
+          } else {
 #pragma unroll
-          for (int hh = 0; hh < HT; ++hh) {
-            if (hh == h) {
-              acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
-              acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
-              acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
-              acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
+            for (int hh = 0; hh < HT; ++hh) {
+              if (hh == h) {
+                acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
+                acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
+                acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
+                acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
+              }
             }
           }
         }
       }
       release_slot(ci);
     }
+    if constexpr (HT > 2) flush_far();
     // Cross-warp sum in two rounds through a buffer of kCWarps/2 slots.
     constexpr int kHalf = kCWarps / 2;
     if (warp >= kHalf && cv) {
