@@ -105,18 +105,8 @@ __device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<floa
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 }
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-// Three (two) independent warp reductions interleaved: the same trees as
-// warp_max / warp_sum, one latency chain instead of several.
+// Three (two) independent butterfly reductions over the warp, interleaved so
+// that they share one latency chain.
 __device__ __forceinline__ void warp_max3(float& a, float& b, float& c) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -654,7 +644,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     }
     if (!csync()) { fail(g); return; }
 
-    // ---- C: values and the far numerators.
+    // ---- C: values and the far numerators.  With one or two heads the V
+    // and T^ row loops are unrolled (more loads in flight per warp); with
+    // more heads the registers are better spent on the head accumulators.
     const bool cv = lane < (dv >> 2);
     float4 acc[HT];
 #pragma unroll
@@ -664,6 +656,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       const float* stage = reinterpret_cast<const float*>(stage_ptr(ci));
       const int r0 = st * P.rows_v;
       const int nrow = min(P.rows_v, ns + w - r0);
+#pragma unroll (HT <= 2 ? 4 : 1)
       for (int lr = warp; lr < nrow; lr += kCWarps) {
         const int j = r0 + lr;  // near row: sinks first, then window slots
         if (j < nnear && cv) {
@@ -722,6 +715,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           reinterpret_cast<const uint16_t*>(stage + (size_t)P.rows_t * dv * 4);
       const int r0 = st * P.rows_t;
       const int nrow = min(P.rows_t, H * m - r0);
+#pragma unroll (HT <= 2 ? 2 : 1)
       for (int lr = warp; lr < nrow; lr += kCWarps) {
         const int h = th, b = tb;
         tb += kCWarps;
