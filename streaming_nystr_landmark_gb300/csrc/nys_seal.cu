@@ -194,11 +194,12 @@ __host__ __device__ inline size_t pinv_smem_doubles(int me) {
   return 3 * (size_t)me * me + 2 * (size_t)me * kTileStride;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) {
   extern __shared__ __align__(16) double dsm[];
   __shared__ int fail;
   __shared__ double lam_s, mean_diag_s;
+  __shared__ double rdiag[kMaxM];  // 1 / L_jj: one f64 division per column
   const int tid = threadIdx.x;
   const int H = s.heads, m = s.m, d = s.d;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
@@ -209,23 +210,39 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   double* A = dsm;            // [me][me]
   double* G = A + me * me;    // [me][me]  A^T A
   double* Lf = G + me * me;   // [me][me]  Cholesky factor / working copy
-  double* Qt = Lf + me * me;  // [me][kTileStride]
-  double* Kt = Qt + me * kTileStride;
+  // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x).
+  float* Qh = reinterpret_cast<float*>(Lf + me * me);  // [me][kTileStride] each
+  float* Ql = Qh + me * kTileStride;
+  float* Kh = Ql + me * kTileStride;
+  float* Kl = Kh + me * kTileStride;
   const double* K64 = ws + (gi * (1 + H)) * (int64_t)m * d;
   const double* Q64 = ws + (gi * (1 + H) + 1 + h) * (int64_t)m * d;
   const double scale = (double)s.scale;
 
-  // A[i][j] = exp((q~64_i . k~64_j) * scale)
+  // A[i][j] = exp((q~64_i . k~64_j) * scale).  The dot product runs in
+  // double-float arithmetic on the fp32 pipe (GB300's f64 rate is a small
+  // fraction of its f32 rate): hi*hi exactly by FMA two-product, the cross
+  // terms hi*lo + lo*hi into its error, Knuth two-sum into an unevaluated
+  // (sh, sl) pair.  Relative to sum|q_c k_c| the result is within ~1e-13 of
+  // the f64 dot product; exp and everything after run in f64.
   constexpr int kPer = (kMaxM * kMaxM + kThreads - 1) / kThreads;
-  double acc[kPer];
+  float sh[kPer], sl[kPer];
 #pragma unroll
-  for (int p = 0; p < kPer; ++p) acc[p] = 0.0;
+  for (int p = 0; p < kPer; ++p) {
+    sh[p] = 0.f;
+    sl[p] = 0.f;
+  }
   for (int c0 = 0; c0 < d; c0 += kTile) {
     const int cw = min(kTile, d - c0);
     for (int idx = tid; idx < me * kTile; idx += kThreads) {
       const int i = idx / kTile, cc = idx - i * kTile;
-      Qt[i * kTileStride + cc] = cc < cw ? Q64[(int64_t)i * d + c0 + cc] : 0.0;
-      Kt[i * kTileStride + cc] = cc < cw ? K64[(int64_t)i * d + c0 + cc] : 0.0;
+      const double q = cc < cw ? Q64[(int64_t)i * d + c0 + cc] : 0.0;
+      const double kk = cc < cw ? K64[(int64_t)i * d + c0 + cc] : 0.0;
+      const float qh = (float)q, kh = (float)kk;
+      Qh[i * kTileStride + cc] = qh;
+      Ql[i * kTileStride + cc] = (float)(q - (double)qh);
+      Kh[i * kTileStride + cc] = kh;
+      Kl[i * kTileStride + cc] = (float)(kk - (double)kh);
     }
     __syncthreads();
 #pragma unroll
@@ -233,10 +250,22 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       const int pair = tid + p * kThreads;
       if (pair < me * me) {
         const int i = pair / me, j = pair - i * me;
-        double a = acc[p];
-        for (int cc = 0; cc < cw; ++cc)
-          a = fma(Qt[i * kTileStride + cc], Kt[j * kTileStride + cc], a);
-        acc[p] = a;
+        const float* qh = Qh + i * kTileStride;
+        const float* ql = Ql + i * kTileStride;
+        const float* kh = Kh + j * kTileStride;
+        const float* kl = Kl + j * kTileStride;
+        float a = sh[p], b = sl[p];
+        for (int cc = 0; cc < cw; ++cc) {
+          const float pr = qh[cc] * kh[cc];
+          float pe = fmaf(qh[cc], kh[cc], -pr);
+          pe = fmaf(qh[cc], kl[cc], fmaf(ql[cc], kh[cc], pe));
+          const float t = a + pr;
+          const float z = t - a;
+          b += ((a - (t - z)) + (pr - z)) + pe;
+          a = t;
+        }
+        sh[p] = a;
+        sl[p] = b;
       }
     }
     __syncthreads();
@@ -244,7 +273,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
 #pragma unroll
   for (int p = 0; p < kPer; ++p) {
     const int pair = tid + p * kThreads;
-    if (pair < me * me) A[pair] = exp(acc[p] * scale);
+    if (pair < me * me) A[pair] = exp(((double)sh[p] + (double)sl[p]) * scale);
   }
   __syncthreads();
 
@@ -277,15 +306,19 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       if (tid == 0) {
         double sp = Lf[j * me + j];
         for (int kk = 0; kk < j; ++kk) sp -= Lf[j * me + kk] * Lf[j * me + kk];
-        if (!(sp > 0.0) || !isfinite(sp)) fail = 1;
-        else Lf[j * me + j] = sqrt(sp);
+        if (!(sp > 0.0) || !isfinite(sp)) {
+          fail = 1;
+        } else {
+          Lf[j * me + j] = sqrt(sp);
+          rdiag[j] = 1.0 / Lf[j * me + j];
+        }
       }
       __syncthreads();
       if (fail) break;
       for (int i = j + 1 + tid; i < me; i += kThreads) {
         double a = Lf[i * me + j];
         for (int kk = 0; kk < j; ++kk) a -= Lf[i * me + kk] * Lf[j * me + kk];
-        Lf[i * me + j] = a / Lf[j * me + j];
+        Lf[i * me + j] = a * rdiag[j];
       }
       __syncthreads();
     }
@@ -307,12 +340,12 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       for (int i = 0; i < me; ++i) {
         double a = A[j * me + i];
         for (int kk = 0; kk < i; ++kk) a -= Lf[i * me + kk] * X[kk * me + j];
-        X[i * me + j] = a / Lf[i * me + i];
+        X[i * me + j] = a * rdiag[i];
       }
       for (int i = me - 1; i >= 0; --i) {
         double a = X[i * me + j];
         for (int kk = i + 1; kk < me; ++kk) a -= Lf[kk * me + i] * X[kk * me + j];
-        X[i * me + j] = a / Lf[i * me + i];
+        X[i * me + j] = a * rdiag[i];
       }
     }
     __syncthreads();
@@ -337,17 +370,20 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
 //           (one float4 of each feeds 4*TR FMAs);
 //   online  per-row block maximum over the 16 lanes of the row group, new
 //   max     running maximum, rescale alpha = exp(old - new), p = exp(L - max);
-//   values  the block's p (reusing the key tile's shared memory, transposed)
-//           times the value tile: part[TR][8] for columns tx*8..tx*8+7;
+//   values  the block's p (row-major in the key tile's shared memory, one
+//           float4 store per row) times the value tile: part[TR][8] for
+//           columns tx*4..tx*4+3 and 64+tx*4..64+tx*4+3 (both float4 reads of
+//           a value row are contiguous over the 16 lanes: no bank conflicts);
 //   fold    (hi, lo) <- (hi, lo) * alpha + part, compensated (comp_axpy), so
 //           that tens of thousands of keys do not accumulate f32 rounding.
 constexpr int kKeyBlock = 64;
 constexpr int kValTile = 128;
 constexpr int kKtStride = kKeyBlock + 4;  // 68: conflict-free transposed stores
+constexpr int kPtStride = kKeyBlock + 4;  // p rows, 16-byte aligned
 
 // The key tile and, after the logits, the probability tile share one region.
 __host__ __device__ inline size_t replay_kt_floats(int rt, int d) {
-  const size_t a = (size_t)d * kKtStride, b = (size_t)kKeyBlock * rt;
+  const size_t a = (size_t)d * kKtStride, b = (size_t)rt * kPtStride;
   return a > b ? a : b;
 }
 __host__ __device__ inline size_t replay_smem_floats(int rt, int d) {
@@ -387,7 +423,7 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   const float scale = s.scale;
   float* QT = fsm;                     // [d][RT]   Q~ transposed, rows >= m_eff zero
   float* KT = QT + (size_t)d * RT;     // [d][kKtStride]  key block transposed
-  float* PT = KT;                      // [kKeyBlock][RT] p, after the logits
+  float* PT = KT;                      // [RT][kPtStride] p, after the logits
   float* VB = KT + replay_kt_floats(RT, d);  // [kKeyBlock][kValTile]
 
   const float* qsrc = s.q_tilde + hb * m * (int64_t)d;
@@ -488,9 +524,9 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
     }
     __syncthreads();  // every thread is done reading KT: p takes its place
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int i = 0; i < TR; ++i) PT[(tx * 4 + j) * RT + ty * TR + i] = L[i][j];
+    for (int i = 0; i < TR; ++i)
+      *reinterpret_cast<float4*>(PT + (ty * TR + i) * kPtStride + tx * 4) =
+          make_float4(L[i][0], L[i][1], L[i][2], L[i][3]);
     __syncthreads();
 
     float part[TR][8];
@@ -498,12 +534,12 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
     for (int i = 0; i < TR; ++i)
 #pragma unroll
       for (int c = 0; c < 8; ++c) part[i][c] = 0.f;
-#pragma unroll 4
-    for (int jj = 0; jj < kKeyBlock; ++jj) {
-      float a[TR];
-      load_rows<TR>(PT + jj * RT + ty * TR, a);
-      const float4 b0 = *reinterpret_cast<const float4*>(VB + jj * kValTile + tx * 8);
-      const float4 b1 = *reinterpret_cast<const float4*>(VB + jj * kValTile + tx * 8 + 4);
+    // One key of the value contraction: p of this thread's rows times the
+    // key's two value chunks.
+    auto pv_key = [&](const float (&a)[TR], int jj) {
+      const float* vr = VB + jj * kValTile + tx * 4;
+      const float4 b0 = *reinterpret_cast<const float4*>(vr);
+      const float4 b1 = *reinterpret_cast<const float4*>(vr + kValTile / 2);
 #pragma unroll
       for (int i = 0; i < TR; ++i) {
         part[i][0] = fmaf(a[i], b0.x, part[i][0]);
@@ -515,6 +551,22 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
         part[i][6] = fmaf(a[i], b1.z, part[i][6]);
         part[i][7] = fmaf(a[i], b1.w, part[i][7]);
       }
+    };
+    for (int jj = 0; jj < kKeyBlock; jj += 4) {
+      // p of four consecutive keys for each row: one broadcast float4 each.
+      float ax[TR], ay[TR], az[TR], aw[TR];
+#pragma unroll
+      for (int i = 0; i < TR; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(PT + (ty * TR + i) * kPtStride + jj);
+        ax[i] = t4.x;
+        ay[i] = t4.y;
+        az[i] = t4.z;
+        aw[i] = t4.w;
+      }
+      pv_key(ax, jj);
+      pv_key(ay, jj + 1);
+      pv_key(az, jj + 2);
+      pv_key(aw, jj + 3);
     }
 #pragma unroll
     for (int i = 0; i < TR; ++i)
@@ -540,7 +592,7 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
     uint16_t* ldst = s.t_lo + (hb * m + row) * (int64_t)dv + c0;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const int col = tx * 8 + c;
+      const int col = (c < 4 ? 0 : kValTile / 2 - 4) + tx * 4 + c;
       if (col < cw) {
         tdst[col] = hi[i][c];
         ldst[col] = (uint16_t)(pack_bf16x2(lo[i][c], 0.f) & 0xffffu);
