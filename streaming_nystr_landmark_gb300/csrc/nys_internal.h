@@ -228,6 +228,16 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
                              int max_me, const float* q, const float* k, const float* v,
                              double* ws, cudaStream_t stream);
 
+// Tensor-core replay (nys_replay_tc.cu): whether the geometry fits it
+// (m >= 32, d and dv <= 128 in multiples of 32), and its launch.  It takes
+// the groups whose replay folds at least kReplayTcMinKeys keys; the CUDA-core
+// replay takes the others (its per-CTA setup is cheaper for short prompts),
+// so a group's result does not depend on the batch it is sealed in.
+constexpr int kReplayTcMinKeys = 256;
+bool replay_tc_fits(const DevState& s);
+cudaError_t launch_replay_tc(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
+                             const float* k, const float* v, cudaStream_t stream);
+
 // Host-side checks of a seal request, identical to nys_seal's, for entry
 // points that supply their own workspace.  Fills the device view and m_eff
 // (printing the one-time clamp notice); returns a nys_status.

@@ -406,7 +406,7 @@ __device__ __forceinline__ void load_rows(const float* p, float (&a)[TR]) {
 template <int TR>
 __global__ void __launch_bounds__(kThreads, 2)
 replay_kernel(DevState s, int64_t g0, SealGeom sg,
-              const float* __restrict__ k, const float* __restrict__ v) {
+              const float* __restrict__ k, const float* __restrict__ v, int skip_long) {
   constexpr int RT = 16 * TR;
   extern __shared__ __align__(16) float fsm[];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -418,6 +418,7 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   int t, me;
   int64_t off;
   seal_geom(sg, gi, t, me, off);
+  if (skip_long && t - w - ns >= kReplayTcMinKeys) return;  // the tensor-core replay's
   const int c0 = blockIdx.y * kValTile;
   const int cw = min(kValTile, dv - c0);
   const float scale = s.scale;
@@ -603,13 +604,13 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
 
 template <int TR>
 cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
-                          const float* k, const float* v, cudaStream_t stream) {
+                          const float* k, const float* v, int skip_long, cudaStream_t stream) {
   const size_t bytes = replay_smem_floats(16 * TR, s.d) * sizeof(float);
   cudaError_t e = ensure_smem<replay_kernel<TR>>(bytes);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
   replay_kernel<TR><<<dim3((unsigned)(n * s.heads), tiles), kThreads, bytes, stream>>>(
-      s, g0, sg, k, v);
+      s, g0, sg, k, v, skip_long);
   return cudaGetLastError();
 }
 
@@ -633,9 +634,21 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
   pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, sg, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  if (max_me <= 16) return launch_replay<1>(s, g0, n, sg, k, v, stream);
-  if (max_me <= 32) return launch_replay<2>(s, g0, n, sg, k, v, stream);
-  return launch_replay<4>(s, g0, n, sg, k, v, stream);
+  // Replay: tensor cores for groups with long prompts (where the geometry
+  // fits), CUDA cores for the rest.  A uniform batch launches only the path
+  // its prompt length takes; a ragged one launches both, and each skips the
+  // other's groups.
+  const bool tc = replay_tc_fits(s);
+  const bool uniform = sg.t_arr == nullptr;
+  const bool long_prompt = sg.t - s.w - s.sink >= kReplayTcMinKeys;
+  if (tc && (!uniform || long_prompt)) {
+    if ((e = launch_replay_tc(s, g0, n, sg, k, v, stream)) != cudaSuccess) return e;
+    if (uniform) return cudaSuccess;
+  }
+  const int skip_long = tc ? 1 : 0;
+  if (max_me <= 16) return launch_replay<1>(s, g0, n, sg, k, v, skip_long, stream);
+  if (max_me <= 32) return launch_replay<2>(s, g0, n, sg, k, v, skip_long, stream);
+  return launch_replay<4>(s, g0, n, sg, k, v, skip_long, stream);
 }
 
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
