@@ -140,9 +140,11 @@ typedef struct {
   int32_t t;        /* prompt length the group was sealed with                */
   int32_t win_len;  /* keys in the window (w once sealed)                     */
   int32_t win_head; /* ring slot of the oldest window key                     */
-  int32_t status;   /* 0, or nonzero when a decode launch's bounded wait gave
-                       up before this group was stepped (its state is stale
-                       and its last outputs are not valid)                    */
+  int32_t status;   /* 0 when healthy; 1 when a decode launch's bounded wait
+                       gave up before this group was stepped (its state is
+                       stale and its last outputs are not valid); 3 when the
+                       tensor-core replay of its seal gave up (its far field
+                       is not valid).  Sealing again clears it.              */
 } nys_group_info;
 
 /* Bytes of device memory a handle of n_groups groups needs (nystrom.rs,

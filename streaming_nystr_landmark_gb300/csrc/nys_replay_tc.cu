@@ -17,16 +17,19 @@
 //
 // One CTA of 256 threads per (group, up to 128 landmark rows = 128 / m
 // heads).  Per key block:
-//   1. all threads: K block -> three bf16 planes [key][d], V block ->
-//      three planes of V^T [dv][key], in the K-major no-swizzle layout the
-//      MMA reads (8x8 core matrices of 128 B);
-//   2. one thread: S = Q~ K^T as 6 * d/16 MMAs (M=128, N=64) into TMEM;
+//   1. the K block is in three bf16 planes [key][d] (the K-major no-swizzle
+//      layout the MMA reads: 8x8 core matrices of 128 B), split by
+//      warpgroup 1 from the registers it loaded during the previous block;
+//   2. one thread: S = Q~ K^T as 6 * d/16 MMAs (M=128, N=64) into TMEM,
+//      while all threads split the V block into three planes of V^T
+//      [dv][key];
 //   3. warpgroup 0 (thread = row): S row from TMEM, logits, block max, new
 //      running max, rescale alpha, p = exp(s - m), Z^ fold, p split into
 //      three planes [row][key] in the K block's shared memory;
 //   4. one thread: O = P V as 6 * 4 MMAs (M=128, N=dv) into TMEM;
 //   5. both warpgroups (half the columns each): (hi, lo) <- (hi, lo) * alpha
-//      + O, with hi and lo kept in TMEM.
+//      + O, with hi and lo kept in TMEM; warpgroup 1 then splits the next
+//      K block into the key planes.
 // Every wait on an MMA is bounded (2 s of %globaltimer); a timeout sets the
 // group's status word and the CTA stops, frees its tensor memory and
 // returns.
@@ -254,7 +257,7 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
   const int row = tid & (kTcRows - 1);
   const int half = tid >> 7;  // 0: warps 0-3, 1: warps 4-7
   const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  const int cols_half = dv >> 1;  // a multiple of 8; processed 16 at a time
+  const int cols_half = dv >> 1;  // a multiple of 16; processed 16 at a time
   {
     float z[16];
 #pragma unroll
@@ -464,7 +467,7 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
   }
 
   if (*vabort) {
-    if (tid == 0) s.ints[g * kIntsPerGroup + kIntStatus] = 3;
+    if (tid == 0) s.ints[g * kIntsPerGroup + kIntStatus] = 3;  // replay gave up
   } else {
     // Write this CTA's rows of T^ (hi f32, lo bf16) and Z^, running maxima.
     const int hh = h0 + row / m, i = row - (row / m) * m;
