@@ -277,12 +277,18 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   }
   __syncthreads();
 
-  // G = A^T A
-  for (int pair = tid; pair < me * me; pair += kThreads) {
-    const int i = pair / me, j = pair - i * me;
+  // G = A^T A, symmetric: the lower triangle (j <= i) enumerated densely so
+  // that every lane has a pair, each entry mirrored.
+  const int tri = me * (me + 1) / 2;
+  for (int p = tid; p < tri; p += kThreads) {
+    int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
+    while (i * (i + 1) / 2 > p) --i;
+    while ((i + 1) * (i + 2) / 2 <= p) ++i;
+    const int j = p - i * (i + 1) / 2;
     double a = 0.0;
     for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
-    G[pair] = a;
+    G[i * me + j] = a;
+    G[j * me + i] = a;
   }
   __syncthreads();
   if (tid == 0) {
