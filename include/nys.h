@@ -283,6 +283,14 @@ int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n);
  * waits on anything.  Errors: NYS_E_INVAL. */
 int nys_debug_stall_once(nys_states* st, int32_t stage);
 
+/* Test hook, no counterpart on the pages: in the next nys_seal on this
+ * handle, the tensor-core replay (groups whose prompt leaves >= 256 keys to
+ * fold, m >= 32) skips issuing the first MMAs of its first CTA, so that
+ * CTA's bounded waits run out after 2 s and its group's status word becomes
+ * 3.  Exercises the replay's timeout path without faulting or hanging the
+ * GPU; sealing again clears the status.  Errors: NYS_E_INVAL. */
+int nys_debug_stall_replay_once(nys_states* st);
+
 /* The geometry a handle was created with.  Errors: NYS_E_INVAL. */
 int nys_config_of(const nys_states* st, nys_config* cfg, int64_t* n_groups);
 

@@ -22,6 +22,7 @@ struct nys_states {
   std::vector<int32_t> exact_len;  // keys held by exact-only groups, -1 otherwise
   int64_t n_exact;                 // how many groups are exact-only
   int debug_skip;                  // test hook for the next decode launch
+  int debug_replay;                // test hook for the next seal's replay
   int device;
 };
 
@@ -248,6 +249,7 @@ int nys_alloc_states(const nys_config* cfg, int64_t n_groups, void* dev_buf,
   st->exact_len.assign((size_t)n_groups, -1);
   st->n_exact = 0;
   st->debug_skip = -1;
+  st->debug_replay = 0;
   *out = st;
   return NYS_OK;
 }
@@ -305,11 +307,13 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
   if (cudaMallocAsync(&ws, per * (size_t)chunk, s) != cudaSuccess) return NYS_E_CUDA;
   cudaError_t e = cudaSuccess;
   const int64_t H = c.heads_per_kv;
+  const int stall = st->debug_replay;
+  st->debug_replay = 0;
   for (int64_t a = 0; a < n && e == cudaSuccess; a += chunk) {
     const int64_t nb = std::min(chunk, n - a);
     e = nys::launch_seal(ds, g0 + a, nb, t, m_eff, q + a * H * (int64_t)t * c.d,
                          k + a * (int64_t)t * c.d, v + a * (int64_t)t * c.dv,
-                         static_cast<double*>(ws), s);
+                         static_cast<double*>(ws), s, a == 0 ? stall : 0);
   }
   const cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess || ef != cudaSuccess) return NYS_E_CUDA;
@@ -464,6 +468,12 @@ int nys_mark_sealed(nys_states* st, int64_t g0, int64_t n) {
 int nys_debug_stall_once(nys_states* st, int32_t stage) {
   if (!st || stage < 0) return NYS_E_INVAL;
   st->debug_skip = stage;
+  return NYS_OK;
+}
+
+int nys_debug_stall_replay_once(nys_states* st) {
+  if (!st) return NYS_E_INVAL;
+  st->debug_replay = 1;
   return NYS_OK;
 }
 

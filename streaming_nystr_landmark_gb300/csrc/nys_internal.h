@@ -217,16 +217,19 @@ size_t seal_workspace_bytes_per_group(const DevState& s);
 // Seal groups [g0, g0+n) with prompt length t and m_eff landmarks, using
 // `ws` (seal_workspace_bytes_per_group * n bytes) as f64 scratch.  Three
 // kernel launches on `stream`.
+// debug_stall (test hook): the tensor-core replay's first CTA withholds its
+// first MMA, so its bounded waits run out (status 3 for its group).
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
-                        const float* v, double* ws, cudaStream_t stream);
+                        const float* v, double* ws, cudaStream_t stream,
+                        int debug_stall = 0);
 
 // Seal with per-group prompt geometry (sg's arrays on the device, indexed
 // from 0 for group g0); max_me bounds every group's m_eff.  q, k, v point at
 // the start of the packed batch.
 cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
                              int max_me, const float* q, const float* k, const float* v,
-                             double* ws, cudaStream_t stream);
+                             double* ws, cudaStream_t stream, int debug_stall = 0);
 
 // Tensor-core replay (nys_replay_tc.cu): whether the geometry fits it
 // (m >= 32, d and dv <= 128 in multiples of 32), and its launch.  It takes
@@ -236,7 +239,8 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
 constexpr int kReplayTcMinKeys = 256;
 bool replay_tc_fits(const DevState& s);
 cudaError_t launch_replay_tc(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
-                             const float* k, const float* v, cudaStream_t stream);
+                             const float* k, const float* v, cudaStream_t stream,
+                             int debug_stall = 0);
 
 // Host-side checks of a seal request, identical to nys_seal's, for entry
 // points that supply their own workspace.  Fills the device view and m_eff

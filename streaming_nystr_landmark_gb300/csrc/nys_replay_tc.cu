@@ -196,7 +196,8 @@ __device__ __constant__ int kPairB[6] = {0, 1, 0, 2, 1, 0};
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ k,
-                 const float* __restrict__ v, int heads_per_cta, int ctas_per_group) {
+                 const float* __restrict__ v, int heads_per_cta, int ctas_per_group,
+                 int debug_stall) {
   extern __shared__ __align__(1024) unsigned char tsm[];
   __shared__ __align__(8) uint64_t bar_s, bar_o;
   __shared__ uint32_t tmem_slot;
@@ -322,8 +323,9 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // 2. S = Q~ K^T, issued by one thread ...
-    if (tid == 0) {
+    // 2. S = Q~ K^T, issued by one thread ...  (test hook: the first CTA
+    //    withholds its first block's MMAs, so its waits run out)
+    if (tid == 0 && !(debug_stall && blockIdx.x == 0 && j0 == ns)) {
       uint32_t acc = 0;
       for (int ks = 0; ks < (d >> 4); ++ks)
         for (int pr = 0; pr < 6; ++pr) {
@@ -514,7 +516,8 @@ bool replay_tc_fits(const DevState& s) {
 }
 
 cudaError_t launch_replay_tc(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
-                             const float* k, const float* v, cudaStream_t stream) {
+                             const float* k, const float* v, cudaStream_t stream,
+                             int debug_stall) {
   if (n <= 0) return cudaSuccess;
   const int heads_per_cta = kTcRows / s.m < s.heads ? kTcRows / s.m : s.heads;
   const int ctas_per_group = (s.heads + heads_per_cta - 1) / heads_per_cta;
@@ -522,7 +525,7 @@ cudaError_t launch_replay_tc(const DevState& s, int64_t g0, int64_t n, const Sea
   cudaError_t e = ensure_smem<replay_tc_kernel>(bytes);
   if (e != cudaSuccess) return e;
   replay_tc_kernel<<<(unsigned)(n * ctas_per_group), kTcThreads, bytes, stream>>>(
-      s, g0, sg, k, v, heads_per_cta, ctas_per_group);
+      s, g0, sg, k, v, heads_per_cta, ctas_per_group, debug_stall);
   return cudaGetLastError();
 }
 

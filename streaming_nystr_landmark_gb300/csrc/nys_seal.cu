@@ -628,7 +628,7 @@ size_t seal_workspace_bytes_per_group(const DevState& s) {
 
 cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
                              int max_me, const float* q, const float* k, const float* v,
-                             double* ws, cudaStream_t stream) {
+                             double* ws, cudaStream_t stream, int debug_stall) {
   if (n <= 0) return cudaSuccess;
   cudaError_t e;
   landmarks_kernel<<<dim3((unsigned)n, 1 + s.heads), kThreads, 0, stream>>>(s, g0, sg, q, k, v,
@@ -648,7 +648,7 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
   const bool uniform = sg.t_arr == nullptr;
   const bool long_prompt = sg.t - s.w - s.sink >= kReplayTcMinKeys;
   if (tc && (!uniform || long_prompt)) {
-    if ((e = launch_replay_tc(s, g0, n, sg, k, v, stream)) != cudaSuccess) return e;
+    if ((e = launch_replay_tc(s, g0, n, sg, k, v, stream, debug_stall)) != cudaSuccess) return e;
     if (uniform) return cudaSuccess;
   }
   const int skip_long = tc ? 1 : 0;
@@ -659,9 +659,9 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
 
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
-                        const float* v, double* ws, cudaStream_t stream) {
+                        const float* v, double* ws, cudaStream_t stream, int debug_stall) {
   const SealGeom sg{t, m_eff, nullptr, nullptr, nullptr};
-  return launch_seal_geom(s, g0, n, sg, m_eff, q, k, v, ws, stream);
+  return launch_seal_geom(s, g0, n, sg, m_eff, q, k, v, ws, stream, debug_stall);
 }
 
 }  // namespace nys

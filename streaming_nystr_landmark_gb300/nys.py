@@ -35,7 +35,8 @@ EXPORTED = ("nys_memory_bytes", "nys_alloc_states", "nys_free_states",
             "nys_mark_sealed", "nys_config_of", "nys_strerror",
             "nys_seal_static", "nys_seal_ragged", "nys_o1_begin", "nys_o1_push_q",
             "nys_o1_seal", "nys_o1_sealed", "nys_o1_step", "nys_o1_memory_bytes",
-            "nys_o1_states", "nys_o1_free", "nys_debug_stall_once")
+            "nys_o1_states", "nys_o1_free", "nys_debug_stall_once",
+            "nys_debug_stall_replay_once")
 
 
 class NysConfig(ctypes.Structure):
@@ -93,6 +94,7 @@ def _load():
         "nys_o1_states": [VP, P(VP)],
         "nys_o1_free": [VP],
         "nys_debug_stall_once": [VP, I32],
+        "nys_debug_stall_replay_once": [VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -180,6 +182,10 @@ def nys_query(handle, g, heads, stream=0):
 
 def nys_debug_stall_once(handle, stage):
     _check(_lib.nys_debug_stall_once(handle, stage), "nys_debug_stall_once")
+
+
+def nys_debug_stall_replay_once(handle):
+    _check(_lib.nys_debug_stall_replay_once(handle), "nys_debug_stall_replay_once")
 
 
 def nys_layout_of(handle):
@@ -299,6 +305,11 @@ class NystromStates:
         """Test hook: the next step's first CTA withholds ring stage `stage`,
         so its bounded waits run out and its groups report status 1."""
         nys_debug_stall_once(self.handle, stage)
+
+    def debug_stall_replay_once(self):
+        """Test hook: the next seal's tensor-core replay withholds its first
+        CTA's first MMAs; that group reports status 3."""
+        nys_debug_stall_replay_once(self.handle)
 
     def region(self, name):
         """A torch view of one state region, shaped as nys_layout documents."""

@@ -85,6 +85,7 @@ def test_bad_rect_and_null_handle():
     assert lib.nys_step_batch(None, 0, 1, None, None, None, None, None) == nys.NYS_E_INVAL
     assert lib.nys_mark_sealed(None, 0, 1) == nys.NYS_E_INVAL
     assert lib.nys_debug_stall_once(None, 0) == nys.NYS_E_INVAL
+    assert lib.nys_debug_stall_replay_once(None) == nys.NYS_E_INVAL
     assert lib.nys_free_states(None) == nys.NYS_OK
     assert lib.nys_memory_bytes(None, 1, None) == nys.NYS_E_INVAL
 

@@ -76,3 +76,36 @@ def test_stalled_stage_times_out_and_marks_its_groups(cuda_device):
     finally:
         for st in states:
             st.close()
+
+
+def test_stalled_replay_times_out_and_marks_its_group(cuda_device):
+    """The tensor-core seal replay's bounded waits: its first CTA withholds
+    its first MMAs (nys_debug_stall_replay_once), waits out its 2 s limit,
+    marks its group (status 3), frees its tensor memory and returns."""
+    import torch
+    # m >= 32 and 300 - 16 - 4 = 280 keys to fold: the tensor-core replay.
+    wl = Workload("replay_stall", 2, 32, 32, 32, 16, 4, 0, 300, 4, 1, 1, 4,
+                  "unit2", seed=23)
+    q, k, v, _ = host_prompt_batch(wl, range(4))
+    q, k, v = (torch.from_numpy(a).to(cuda_device) for a in (q, k, v))
+    states = [nys.NystromStates(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.d, wl.dv,
+                                4, wl.rect, cuda_device) for _ in range(2)]
+    a, b = states
+    try:
+        a.debug_stall_replay_once()
+        for st in states:
+            st.seal(q, k, v)
+        torch.cuda.synchronize()  # the stalled CTA returned: the context is alive
+        assert list(_status(a)) == [3, 0, 0, 0]
+        assert not _status(b).any()
+        assert a.query(0)[0]["status"] == 3
+        for name in ("t_hat", "t_lo", "z_hat", "z_lo", "m_max", "mu", "k_tilde"):
+            assert torch.equal(a.region(name)[1:], b.region(name)[1:]), name
+        a.seal(q, k, v)  # a fresh seal clears the status
+        torch.cuda.synchronize()
+        assert not _status(a).any()
+        for name in ("t_hat", "t_lo", "z_hat", "z_lo", "m_max", "mu"):
+            assert torch.equal(a.region(name), b.region(name)), name
+    finally:
+        for st in states:
+            st.close()
