@@ -94,6 +94,23 @@ __device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, 
   nlo = t - (nhi - s);
 }
 
+// Kahan's compensated update of the running sum hi + lo by one term x * y,
+// after an optional rescale by r: lo carries the rounding error of the
+// running sum (recovered by Fast2Sum), so many steps drift no more than a
+// rounding or two.  Five operations when r == 1 against comp_axpy's twelve;
+// the rescale's own rounding error is recovered exactly by FMA.
+__device__ __forceinline__ void kahan_axpy(float& hi, float& lo, float r, float x, float y) {
+  if (r != 1.f) {
+    const float a = hi * r;
+    lo = fmaf(lo, r, fmaf(hi, r, -a));
+    hi = a;
+  }
+  const float yv = fmaf(x, y, lo);
+  const float t = hi + yv;
+  lo = yv - (t - hi);
+  hi = t;
+}
+
 // comp_axpy with r == 1, for callers that branch on r once for many elements.
 __device__ __forceinline__ void comp_add(float hi, float lo, float x, float y, float& nhi,
                                          float& nlo) {

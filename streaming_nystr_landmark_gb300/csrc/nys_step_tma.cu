@@ -737,28 +737,16 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             const float r = rs[h * P.mp + b], e = es[h * P.mp + b];
             float* thp;
             uint16_t* tlp;
+            // Compensated far update (Kahan form, see kahan_axpy).
+            kahan_axpy(x.x, lo.x, r, e, ve.x);
+            kahan_axpy(x.y, lo.y, r, e, ve.y);
+            kahan_axpy(x.z, lo.z, r, e, ve.z);
+            kahan_axpy(x.w, lo.w, r, e, ve.w);
             if constexpr (HT > 2) {
-              // Many heads: the compensated update branches once per row on
-              // r (no new running maximum is the common case).
-              if (r == 1.f) {
-                comp_add(x.x, lo.x, e, ve.x, x.x, lo.x);
-                comp_add(x.y, lo.y, e, ve.y, x.y, lo.y);
-                comp_add(x.z, lo.z, e, ve.z, x.z, lo.z);
-                comp_add(x.w, lo.w, e, ve.w, x.w, lo.w);
-              } else {
-                comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
-                comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
-                comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
-                comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
-              }
               const int row = r0 + lr;  // = h * m + b
               thp = t_hi_g + (size_t)row * dv;
               tlp = t_lo_g + (size_t)row * dv;
             } else {
-              comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
-              comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
-              comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
-              comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
               const int64_t grow = (g * H + h) * (int64_t)m + b;
               thp = s.t_hat + grow * dv + 4 * lane;
               tlp = s.t_lo + grow * dv + 4 * lane;
