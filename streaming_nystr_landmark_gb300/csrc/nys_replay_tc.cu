@@ -28,8 +28,8 @@
 //      three planes [row][key] in the K block's shared memory;
 //   4. one thread: O = P V as 6 * 4 MMAs (M=128, N=dv) into TMEM;
 //   5. both warpgroups (half the columns each): (hi, lo) <- (hi, lo) * alpha
-//      + O, with hi and lo kept in TMEM; warpgroup 1 then splits the next
-//      K block into the key planes.
+//      + O (Kahan-compensated), with hi and lo kept in TMEM; warpgroup 1
+//      then splits the next K block into the key planes.
 // Every wait on an MMA is bounded (2 s of %globaltimer); a timeout sets the
 // group's status word and the CTA stops, frees its tensor memory and
 // returns.
@@ -430,30 +430,13 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
     // 5. (hi, lo) <- (hi, lo) * alpha + O on this thread's column half.
     if (ok) {
       const float alpha = alpha_s[row];
-      // No row of this warp has a new running maximum: the common case.
-      const bool plain = __all_sync(0xffffffffu, alpha == 1.f);
       for (int c = half * cols_half; c < (half + 1) * cols_half; c += 16) {
         float o[16], hi[16], lo[16];
         tc_ld16(lane_base + kColO + c, o);
         tc_ld16(lane_base + kColHi + c, hi);
         tc_ld16(lane_base + kColLo + c, lo);
-        if (plain) {
 #pragma unroll
-          for (int jx = 0; jx < 16; ++jx) {
-            float nh, nl;
-            comp_add(hi[jx], lo[jx], o[jx], 1.f, nh, nl);
-            hi[jx] = nh;
-            lo[jx] = nl;
-          }
-        } else {
-#pragma unroll
-          for (int jx = 0; jx < 16; ++jx) {
-            float nh, nl;
-            comp_axpy(hi[jx], lo[jx], alpha, o[jx], 1.f, nh, nl);
-            hi[jx] = nh;
-            lo[jx] = nl;
-          }
-        }
+        for (int jx = 0; jx < 16; ++jx) kahan_axpy(hi[jx], lo[jx], alpha, o[jx], 1.f);
         tc_st16(lane_base + kColHi + c, hi);
         tc_st16(lane_base + kColLo + c, lo);
       }

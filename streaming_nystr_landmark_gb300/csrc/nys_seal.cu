@@ -380,7 +380,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
 //           float4 store per row) times the value tile: part[TR][8] for
 //           columns tx*4..tx*4+3 and 64+tx*4..64+tx*4+3 (both float4 reads of
 //           a value row are contiguous over the 16 lanes: no bank conflicts);
-//   fold    (hi, lo) <- (hi, lo) * alpha + part, compensated (comp_axpy), so
+//   fold    (hi, lo) <- (hi, lo) * alpha + part, compensated (kahan_axpy), so
 //           that tens of thousands of keys do not accumulate f32 rounding.
 constexpr int kKeyBlock = 64;
 constexpr int kValTile = 128;
@@ -579,10 +579,7 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
     for (int i = 0; i < TR; ++i)
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        float nh, nl;
-        comp_axpy(hi[i][c], lo[i][c], alpha[i], part[i][c], 1.f, nh, nl);
-        hi[i][c] = nh;
-        lo[i][c] = nl;
+        kahan_axpy(hi[i][c], lo[i][c], alpha[i], part[i][c], 1.f);
       }
   }
 

@@ -327,10 +327,10 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
               if (full) {
                 const float r = rs[hh * L.mp + b], e = es[hh * L.mp + b];
                 const float4 ve = ld4(vev + 4 * c4);
-                comp_axpy(x.x, lo.x, r, e, ve.x, x.x, lo.x);
-                comp_axpy(x.y, lo.y, r, e, ve.y, x.y, lo.y);
-                comp_axpy(x.z, lo.z, r, e, ve.z, x.z, lo.z);
-                comp_axpy(x.w, lo.w, r, e, ve.w, x.w, lo.w);
+                kahan_axpy(x.x, lo.x, r, e, ve.x);
+                kahan_axpy(x.y, lo.y, r, e, ve.y);
+                kahan_axpy(x.z, lo.z, r, e, ve.z);
+                kahan_axpy(x.w, lo.w, r, e, ve.w);
                 st4(trow + 4 * c4, x);
                 uint2 lw;
                 lw.x = pack_bf16x2(lo.x, lo.y);
