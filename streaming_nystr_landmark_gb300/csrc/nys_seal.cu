@@ -417,25 +417,78 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
 
   float* M = s.mu + (g * H + h) * (int64_t)m * m;
   if (solved) {
-    // G M = A^T, one right-hand side (row j of A) per thread; X reuses G.
-    double* X = G;
+    // G M = A^T by forward (L Y = A^T) then backward (L^T M = Y)
+    // substitution, column-oriented over all threads and in double-float
+    // arithmetic (the f64 pipe is the bottleneck): at pivot k every thread
+    // scales row k by 1/L_kk and updates its own (i, j) entries with it.
+    // Pair arrays: L in place of Lf, the right-hand sides in place of G, the
+    // forward result in the (dead) landmark-tile region.
+    float2* L2 = reinterpret_cast<float2*>(Lf);
+    float2* W = reinterpret_cast<float2*>(G);
+    float2* Y = reinterpret_cast<float2*>(Lf + me * me);  // 2 * me * kTileStride doubles >= me^2
+    __shared__ float2 rd2[kMaxM];
     __syncthreads();
-    for (int j = tid; j < me; j += kThreads) {
-      for (int i = 0; i < me; ++i) {
-        double a = A[j * me + i];
-        for (int kk = 0; kk < i; ++kk) a -= Lf[i * me + kk] * X[kk * me + j];
-        X[i * me + j] = a * rdiag[i];
-      }
-      for (int i = me - 1; i >= 0; --i) {
-        double a = X[i * me + j];
-        for (int kk = i + 1; kk < me; ++kk) a -= Lf[kk * me + i] * X[kk * me + j];
-        X[i * me + j] = a * rdiag[i];
-      }
+    for (int e = tid; e < me * me; e += kThreads) {
+      const int i = e / me, j = e - i * me;
+      const double l = Lf[e];  // read, then overwritten by its own pair
+      L2[e] = make_float2((float)l, (float)(l - (double)(float)l));
+      const double a = A[j * me + i];  // A^T[i][j]
+      W[e] = make_float2((float)a, (float)(a - (double)(float)a));
+    }
+    for (int k = tid; k < me; k += kThreads) {
+      const double r = rdiag[k];
+      rd2[k] = make_float2((float)r, (float)(r - (double)(float)r));
     }
     __syncthreads();
+    // Thread (warp, lane) owns rows warp, warp + 8, ... and columns lane,
+    // lane + 32 (no divisions in the pivot loops).
+    const int wrp = tid >> 5, lan = tid & 31;
+    for (int k = 0; k < me; ++k) {
+      const float2 rk = rd2[k];
+      for (int i = wrp; i < me; i += kThreads / 32)
+      for (int j = lan; j < me; j += 32) {
+        if (i < k) continue;
+        const int e = i * me + j;
+        const float2 wk = W[k * me + j];
+        float yh, yl;
+        df_mul(wk.x, wk.y, rk.x, rk.y, yh, yl);  // y_kj = W_kj / L_kk
+        if (i == k) {
+          Y[e] = make_float2(yh, yl);
+        } else {
+          const float2 lik = L2[i * me + k], w = W[e];
+          float ph, pl;
+          df_mul(lik.x, lik.y, yh, yl, ph, pl);
+          float nh, nl;
+          df_add(w.x, w.y, -ph, -pl, nh, nl);
+          W[e] = make_float2(nh, nl);
+        }
+      }
+      __syncthreads();
+    }
+    for (int k = me - 1; k >= 0; --k) {
+      const float2 rk = rd2[k];
+      for (int i = wrp; i <= k; i += kThreads / 32)
+      for (int j = lan; j < me; j += 32) {
+        const int e = i * me + j;
+        const float2 yk = Y[k * me + j];
+        float xh, xl;
+        df_mul(yk.x, yk.y, rk.x, rk.y, xh, xl);  // m_kj = Y_kj / L_kk
+        if (i == k) {
+          W[e] = make_float2(xh, xl);
+        } else {
+          const float2 lki = L2[k * me + i], y = Y[e];  // (L^T)_ik = L_ki
+          float ph, pl;
+          df_mul(lki.x, lki.y, xh, xl, ph, pl);
+          float nh, nl;
+          df_add(y.x, y.y, -ph, -pl, nh, nl);
+          Y[e] = make_float2(nh, nl);
+        }
+      }
+      __syncthreads();
+    }
     for (int pair = tid; pair < me * me; pair += kThreads) {
       const int i = pair / me, j = pair - i * me;
-      M[i * m + j] = (float)X[pair];
+      M[i * m + j] = W[pair].x + W[pair].y;
     }
   } else {
     const double diag = 1.0 / fmax(mean_diag_s, DBL_MIN);
