@@ -6,7 +6,9 @@ streams, which the oracle also consumes; any other group receives
 device-drawn filler of the same distribution, so full-size launches stay full
 size while the oracle only runs the sampled groups.
 
-Tolerances (derived from fp32 evaluation of the step):
+Tolerances (an fp32 evaluation of the step, measured against the oracle
+before any kernel existed, gives ~1.4e-5 per step on the m = 32 workloads;
+the bounds leave room for that plus the state's accumulated rounding):
   outputs         row-normwise  max|o - o_ref| / max|o_ref| <= 1e-4, except
                   rows where the Aggregate guard sits within 1e-5 of its
                   threshold (either branch is then correct) or where the far
