@@ -81,6 +81,10 @@ def test_long_context_workload_full_size(cuda_device):
     ("m_eff_below_budget", 2, 32, 32, 32, 64, 4, 160, 0, 3),
     ("wide_head", 1, 256, 256, 16, 32, 4, 200, 0, 2),
     ("ragged_tail_129_groups", 2, 32, 32, 8, 16, 4, 64, 0, 129),
+    # Tensor-core seal replay (>= 256 keys to fold, m >= 32) on an uneven
+    # geometry: 2 heads of 48 landmarks in the first CTA's 128 rows, 1 in
+    # the second, d = 96 (three 32-element chunk groups), dv = 64.
+    ("tc_replay_uneven", 3, 96, 64, 48, 64, 4, 400, 0, 3),
 ])
 def test_edge_geometries(cuda_device, geo):
     name, H, d, dv, m, w, sink, t, rect, groups = geo
