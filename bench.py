@@ -528,14 +528,56 @@ def run_seal(args, wl):
         st.close()
         del q, k, v
         torch.cuda.empty_cache()
+    # Roofline of the uniform seal: its fp32-equivalent arithmetic (replay
+    # logits and P V over the evicted keys, the pinv's landmark products,
+    # A^T A, Cholesky and solves) against the fp32 FMA peak derived from
+    # the unit counts and the maximum clock (SMs x 128 lanes x 2 x 2.07 GHz).
+    m_eff = min(max(wl.t // 8, 4), wl.m)
+    n_ev = max(wl.t - wl.w - wl.sink, 0)
+    flop_head = (n_ev * m_eff * 2 * (wl.d + wl.dv)
+                 + 2 * m_eff * m_eff * wl.d + m_eff ** 3 + m_eff ** 3 // 3 + 2 * m_eff ** 3)
+    seal_flop = G * H * flop_head
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * 128 * 2 * 2.07e9 / 1e12
+    achieved = seal_flop / (res["uniform"]["ms"] / 1e3) / 1e12
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"derived: {sms} SMs x 128 fp32 lanes x 2 x 2.07 GHz",
+                "flop_per_seal": seal_flop,
+                "note": "fp32-equivalent work; the replay runs on tensor cores for prompts "
+                        "folding >= 256 keys, the pinv's f64-accurate parts in f64 and "
+                        "double-float"}
     line = {"metric": "Nyström seal ms per batch (uniform vs ragged prompts)",
             "value": res["ragged"]["ms"], "unit": "ms", "higher_is_better": False,
             "n_gpus": 1, "steps": 3, "warmup": args.warmup, "dtype": "f32+f64",
-            "data": "synthetic",
+            "data": "synthetic", "roofline": roofline,
             "config": workload_config(wl, {"ragged_t_range": [int(ts.min()), int(ts.max())],
                                            "uniform": res["uniform"],
                                            "ragged": res["ragged"]})}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_seal_rate(wl, args.cpu_budget)
     print(json.dumps(line), flush=True)
+
+
+def oracle_seal_rate(wl, budget_s):
+    """The fp64 oracle's seal (prefill) rate in prompt tokens per second:
+    whole groups sealed one after another, from the host-drawn inputs of
+    groups 0, 1, ..., until the time budget is spent (at least one group)."""
+    from oracle import NystromOracle
+    from streaming_nystr_landmark_gb300.workloads import GroupInputs
+    tokens, spent, groups = 0, 0.0, 0
+    while groups == 0 or (spent < budget_s and groups < wl.n_groups):
+        q, k, v = GroupInputs(wl, groups).prompt()
+        o = NystromOracle(m=wl.m, w=wl.w, sink=wl.sink, heads=wl.heads_per_kv, rect=wl.rect,
+                          d=wl.d, dv=wl.dv)
+        t0 = time.perf_counter()
+        o.prefill(q, k, v)
+        spent += time.perf_counter() - t0
+        tokens += wl.t
+        groups += 1
+    return {"value": tokens / spent, "unit": "prompt tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{groups} group(s) of {wl.t} tokens sealed in {spent:.1f} s; fp64 numpy "
+                      f"oracle (streaming form), 1 thread"}
 
 
 def main():

@@ -261,8 +261,15 @@ __device__ double df_exp(float xh, float xl) {
   return ldexp((double)sh + (double)sl, (int)k);
 }
 
+// Shared memory of the pinv kernel: A (later the forward-solve result), the
+// Cholesky region (first the logit tiles), the right-hand sides.  About
+// 98 KB at m = 64, so two CTAs share an SM.
+__host__ __device__ inline size_t pinv_lf_doubles(int me) {
+  const size_t a = (size_t)me * me, b = 2 * (size_t)me * kTileStride;
+  return a > b ? a : b;
+}
 __host__ __device__ inline size_t pinv_smem_doubles(int me) {
-  return 3 * (size_t)me * me + 2 * (size_t)me * kTileStride;
+  return 2 * (size_t)me * me + pinv_lf_doubles(me);
 }
 
 __global__ void __launch_bounds__(kThreads, 4)
@@ -278,11 +285,11 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   int t_unused, me;
   int64_t off_unused;
   seal_geom(sg, gi, t_unused, me, off_unused);
-  double* A = dsm;            // [me][me]
-  double* G = A + me * me;    // [me][me]  A^T A
-  double* Lf = G + me * me;   // [me][me]  Cholesky factor / working copy
+  double* A = dsm;                          // [me][me]
+  double* Lf = A + me * me;                 // [me][me]  A^T A + lambda I -> Cholesky factor
+  double* Wd = Lf + pinv_lf_doubles(me);    // [me][me]  right-hand sides -> M
   // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x).
-  float* Qh = reinterpret_cast<float*>(Lf + me * me);  // [me][kTileStride] each
+  float* Qh = reinterpret_cast<float*>(Lf);  // [me][kTileStride] each, before Lf is used
   float* Ql = Qh + me * kTileStride;
   float* Kh = Ql + me * kTileStride;
   float* Kl = Kh + me * kTileStride;
@@ -355,23 +362,27 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   }
   __syncthreads();
 
-  // G = A^T A, symmetric: the lower triangle (j <= i) enumerated densely so
-  // that every lane has a pair, each entry mirrored.
+  // G = A^T A + lambda I into Lf, lower triangle only (all the Cholesky
+  // reads), the triangle enumerated densely so that every lane has a pair.
+  // G itself is not kept: a retry rebuilds it from A (same sums, same
+  // order, so the same values).
   const int tri = me * (me + 1) / 2;
-  for (int p = tid; p < tri; p += kThreads) {
-    int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
-    while (i * (i + 1) / 2 > p) --i;
-    while ((i + 1) * (i + 2) / 2 <= p) ++i;
-    const int j = p - i * (i + 1) / 2;
-    double a = 0.0;
-    for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
-    G[i * me + j] = a;
-    G[j * me + i] = a;
-  }
+  auto build_gram = [&](double lam) {
+    for (int p = tid; p < tri; p += kThreads) {
+      int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
+      while (i * (i + 1) / 2 > p) --i;
+      while ((i + 1) * (i + 2) / 2 <= p) ++i;
+      const int j = p - i * (i + 1) / 2;
+      double a = 0.0;
+      for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
+      Lf[i * me + j] = (i == j) ? a + lam : a;
+    }
+  };
+  build_gram(0.0);
   __syncthreads();
   if (tid == 0) {
     double sd = 0.0;
-    for (int i = 0; i < me; ++i) sd += G[i * me + i];
+    for (int i = 0; i < me; ++i) sd += Lf[i * me + i];
     mean_diag_s = sd / (double)me;
     lam_s = 1e-6 * fmax(mean_diag_s, DBL_MIN);
   }
@@ -380,9 +391,10 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   bool solved = false;
   for (int attempt = 0; attempt < 12 && !solved; ++attempt) {
     const double lam = lam_s;
-    for (int pair = tid; pair < me * me; pair += kThreads) {
-      const int i = pair / me, j = pair - i * me;
-      Lf[pair] = G[pair] + (i == j ? lam : 0.0);
+    if (attempt == 0) {
+      for (int i = tid; i < me; i += kThreads) Lf[i * me + i] += lam;
+    } else {
+      build_gram(lam);
     }
     if (tid == 0) fail = 0;
     __syncthreads();
@@ -421,11 +433,11 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     // substitution, column-oriented over all threads and in double-float
     // arithmetic (the f64 pipe is the bottleneck): at pivot k every thread
     // scales row k by 1/L_kk and updates its own (i, j) entries with it.
-    // Pair arrays: L in place of Lf, the right-hand sides in place of G, the
-    // forward result in the (dead) landmark-tile region.
+    // Pair arrays: L in place of Lf, the right-hand sides in their own
+    // region, the forward result in A's region once W holds A^T.
     float2* L2 = reinterpret_cast<float2*>(Lf);
-    float2* W = reinterpret_cast<float2*>(G);
-    float2* Y = reinterpret_cast<float2*>(Lf + me * me);  // 2 * me * kTileStride doubles >= me^2
+    float2* W = reinterpret_cast<float2*>(Wd);
+    float2* Y = reinterpret_cast<float2*>(A);  // A is dead once W holds A^T
     __shared__ float2 rd2[kMaxM];
     __syncthreads();
     for (int e = tid; e < me * me; e += kThreads) {
