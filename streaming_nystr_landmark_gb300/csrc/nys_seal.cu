@@ -261,15 +261,15 @@ __device__ double df_exp(float xh, float xl) {
   return ldexp((double)sh + (double)sl, (int)k);
 }
 
-// Shared memory of the pinv kernel: A (later the forward-solve result), the
-// Cholesky region (first the logit tiles), the right-hand sides.  About
-// 98 KB at m = 64, so two CTAs share an SM.
+// Shared memory of the pinv kernel: A (later, transposed in place, the
+// right-hand sides and the solution) and the Cholesky region (first the
+// logit tiles).  About 67 KB at m = 64, so three CTAs share an SM.
 __host__ __device__ inline size_t pinv_lf_doubles(int me) {
   const size_t a = (size_t)me * me, b = 2 * (size_t)me * kTileStride;
   return a > b ? a : b;
 }
 __host__ __device__ inline size_t pinv_smem_doubles(int me) {
-  return 2 * (size_t)me * me + pinv_lf_doubles(me);
+  return (size_t)me * me + pinv_lf_doubles(me);
 }
 
 __global__ void __launch_bounds__(kThreads, 4)
@@ -287,7 +287,6 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   seal_geom(sg, gi, t_unused, me, off_unused);
   double* A = dsm;                          // [me][me]
   double* Lf = A + me * me;                 // [me][me]  A^T A + lambda I -> Cholesky factor
-  double* Wd = Lf + pinv_lf_doubles(me);    // [me][me]  right-hand sides -> M
   // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x).
   float* Qh = reinterpret_cast<float*>(Lf);  // [me][kTileStride] each, before Lf is used
   float* Ql = Qh + me * kTileStride;
@@ -431,21 +430,24 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   if (solved) {
     // G M = A^T by forward (L Y = A^T) then backward (L^T M = Y)
     // substitution, column-oriented over all threads and in double-float
-    // arithmetic (the f64 pipe is the bottleneck): at pivot k every thread
-    // scales row k by 1/L_kk and updates its own (i, j) entries with it.
-    // Pair arrays: L in place of Lf, the right-hand sides in their own
-    // region, the forward result in A's region once W holds A^T.
+    // arithmetic (the f64 pipe is the bottleneck), in place: at pivot k
+    // every thread reads row k, scales it by 1/L_kk itself, and updates its
+    // own (i, j) entries; row k keeps its unscaled value until a scaling
+    // pass.  Pair arrays: L in place of Lf, the right-hand sides in place of
+    // A (transposed there).
     float2* L2 = reinterpret_cast<float2*>(Lf);
-    float2* W = reinterpret_cast<float2*>(Wd);
-    float2* Y = reinterpret_cast<float2*>(A);  // A is dead once W holds A^T
+    float2* W = reinterpret_cast<float2*>(A);
     __shared__ float2 rd2[kMaxM];
     __syncthreads();
     for (int e = tid; e < me * me; e += kThreads) {
       const int i = e / me, j = e - i * me;
       const double l = Lf[e];  // read, then overwritten by its own pair
       L2[e] = make_float2((float)l, (float)(l - (double)(float)l));
-      const double a = A[j * me + i];  // A^T[i][j]
-      W[e] = make_float2((float)a, (float)(a - (double)(float)a));
+      if (i <= j) {  // W[i][j] = A^T[i][j] = A[j][i]: swap the pair (i, j), (j, i)
+        const double aij = A[i * me + j], aji = A[j * me + i];
+        W[i * me + j] = make_float2((float)aji, (float)(aji - (double)(float)aji));
+        W[j * me + i] = make_float2((float)aij, (float)(aij - (double)(float)aij));
+      }
     }
     for (int k = tid; k < me; k += kThreads) {
       const double r = rdiag[k];
@@ -455,52 +457,52 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     // Thread (warp, lane) owns rows warp, warp + 8, ... and columns lane,
     // lane + 32 (no divisions in the pivot loops).
     const int wrp = tid >> 5, lan = tid & 31;
-    for (int k = 0; k < me; ++k) {
-      const float2 rk = rd2[k];
-      for (int i = wrp; i < me; i += kThreads / 32)
-      for (int j = lan; j < me; j += 32) {
-        if (i < k) continue;
-        const int e = i * me + j;
-        const float2 wk = W[k * me + j];
-        float yh, yl;
-        df_mul(wk.x, wk.y, rk.x, rk.y, yh, yl);  // y_kj = W_kj / L_kk
-        if (i == k) {
-          Y[e] = make_float2(yh, yl);
-        } else {
-          const float2 lik = L2[i * me + k], w = W[e];
-          float ph, pl;
-          df_mul(lik.x, lik.y, yh, yl, ph, pl);
-          float nh, nl;
-          df_add(w.x, w.y, -ph, -pl, nh, nl);
-          W[e] = make_float2(nh, nl);
+    auto scaled = [&](int k, int j, float& h, float& l) {  // W_kj / L_kk
+      const float2 w = W[k * me + j];
+      df_mul(w.x, w.y, rd2[k].x, rd2[k].y, h, l);
+    };
+    auto update = [&](int i, int j, float2 lik, float yh, float yl) {  // W_ij -= l * y
+      const float2 w = W[i * me + j];
+      float ph, pl, nh, nl;
+      df_mul(lik.x, lik.y, yh, yl, ph, pl);
+      df_add(w.x, w.y, -ph, -pl, nh, nl);
+      W[i * me + j] = make_float2(nh, nl);
+    };
+    for (int k = 0; k < me - 1; ++k) {  // forward: rows below the pivot
+      for (int i = wrp; i < me; i += kThreads / 32) {
+        if (i <= k) continue;
+        const float2 lik = L2[i * me + k];
+        for (int j = lan; j < me; j += 32) {
+          float yh, yl;
+          scaled(k, j, yh, yl);
+          update(i, j, lik, yh, yl);
         }
       }
       __syncthreads();
     }
-    for (int k = me - 1; k >= 0; --k) {
-      const float2 rk = rd2[k];
-      for (int i = wrp; i <= k; i += kThreads / 32)
+    for (int i = wrp; i < me; i += kThreads / 32)  // Y = W / diag(L)
       for (int j = lan; j < me; j += 32) {
-        const int e = i * me + j;
-        const float2 yk = Y[k * me + j];
-        float xh, xl;
-        df_mul(yk.x, yk.y, rk.x, rk.y, xh, xl);  // m_kj = Y_kj / L_kk
-        if (i == k) {
-          W[e] = make_float2(xh, xl);
-        } else {
-          const float2 lki = L2[k * me + i], y = Y[e];  // (L^T)_ik = L_ki
-          float ph, pl;
-          df_mul(lki.x, lki.y, xh, xl, ph, pl);
-          float nh, nl;
-          df_add(y.x, y.y, -ph, -pl, nh, nl);
-          Y[e] = make_float2(nh, nl);
+        float h, l;
+        scaled(i, j, h, l);
+        W[i * me + j] = make_float2(h, l);
+      }
+    __syncthreads();
+    for (int k = me - 1; k > 0; --k) {  // backward: rows above the pivot
+      for (int i = wrp; i < k; i += kThreads / 32) {
+        const float2 lki = L2[k * me + i];  // (L^T)_ik = L_ki
+        for (int j = lan; j < me; j += 32) {
+          float xh, xl;
+          scaled(k, j, xh, xl);
+          update(i, j, lki, xh, xl);
         }
       }
       __syncthreads();
     }
-    for (int pair = tid; pair < me * me; pair += kThreads) {
+    for (int pair = tid; pair < me * me; pair += kThreads) {  // M = W / diag(L)
       const int i = pair / me, j = pair - i * me;
-      M[i * m + j] = W[pair].x + W[pair].y;
+      float h, l;
+      scaled(i, j, h, l);
+      M[i * m + j] = h + l;
     }
   } else {
     const double diag = 1.0 / fmax(mean_diag_s, DBL_MIN);
