@@ -8,15 +8,17 @@
 //     block (g, 1 + h) takes head h's queries -- Q~_h = seg_means(q_h)
 //     (NystromHead::seal).  Segment i covers rows [i t / m_eff,
 //     (i+1) t / m_eff); sums keep f64 accuracy (fn seg_means accumulates in
-//     f64).  The f64 means go to a workspace for step 2, their f32 roundings
-//     to the state.
+//     f64), computed in double-float.  The f64-accurate means go to a
+//     workspace for step 2 as (hi, lo) pairs, their f32 roundings to the
+//     state.
 //  2. pinv_kernel, one block per (group, head): A = exp(Q~64 K~64^T * scale)
-//     in f64, then M = (A^T A + lambda I)^-1 A^T (fn ridge_pinv):
+//     to f64 accuracy, then M = (A^T A + lambda I)^-1 A^T (fn ridge_pinv):
 //     lambda = 1e-6 * max(mean diag(A^T A), DBL_MIN); a failed Cholesky
 //     (pivot not > 0 or not finite, fn cholesky) multiplies lambda by ten, at
 //     most twelve attempts, then M = I / max(mean diag, DBL_MIN).  The
-//     Cholesky and the two triangular solves keep the page's summation order.
-//  3. replay_kernel, one block per (group, head): the replay of positions
+//     Cholesky keeps the page's summation order.
+//  3. replay_kernel (or, for long prompts, replay_tc_kernel in
+//     nys_replay_tc.cu), one block per (group, head): the replay of positions
 //     sink..t-1 through the ring leaves keys sink..t-w-1 in the far field
 //     (NystromState::advance -> NystromHead::far_insert).  The state that
 //     sequential loop produces is m_max_i = max_j l_ij, Z^_i = sum_j
@@ -42,6 +44,34 @@ __device__ __forceinline__ float4 ld4(const float* p) {
 }
 __device__ __forceinline__ void st4(float* p, float4 x) {
   *reinterpret_cast<float4*>(p) = x;
+}
+
+// ---- double-float arithmetic (unevaluated pairs hi + lo of f32) for the
+// parts of the seal that need more than f32: GB300's f32 pipe is tens of
+// times faster than its f64 pipe.
+__device__ __forceinline__ void df_two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float z = s - a;
+  e = (a - (s - z)) + (b - z);
+}
+__device__ __forceinline__ void df_fast_two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  e = b - (s - a);
+}
+__device__ __forceinline__ void df_mul(float ah, float al, float bh, float bl, float& ph,
+                                       float& pl) {
+  const float p = ah * bh;
+  float e = fmaf(ah, bh, -p);
+  e = fmaf(ah, bl, e);
+  e = fmaf(al, bh, e);
+  df_fast_two_sum(p, e, ph, pl);
+}
+__device__ __forceinline__ void df_add(float ah, float al, float bh, float bl, float& sh,
+                                       float& sl) {
+  float s, e;
+  df_two_sum(ah, bh, s, e);
+  e += al + bl;
+  df_fast_two_sum(s, e, sh, sl);
 }
 
 // ---------------------------------------------------------------- 1
@@ -71,10 +101,11 @@ __device__ __forceinline__ void sum8(const float (&x)[8], float& hi, float& lo) 
 // One block per (group, row source): y = 0 reads the group's keys (K~ plus
 // sinks, ring and counters), y = 1 + h head h's queries (Q~_h).  One warp per
 // landmark segment, lanes over float4 columns: no cross-warp reduction.  Rows
-// are summed eight at a time exactly (sum8) and each such partial enters an
-// f64 accumulator with one f64 addition, so the segment sums keep f64
-// accuracy (within ~1e-14 of a sequential f64 sum) at an eighth of the f64
-// additions -- GB300's f64 rate, not HBM, bounds a plain f64 loop here.
+// are summed eight at a time exactly (sum8) and each such partial enters a
+// double-float (hi, lo) accumulator; the mean is the pair divided by the
+// segment length (exact remainder by FMA).  The segment means keep f64
+// accuracy (~1e-14 of a sequential f64 sum) with no f64 operation: GB300's
+// f64 rate, not HBM, bounded even one f64 addition per eight rows here.
 __global__ void __launch_bounds__(kThreads)
 landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
                  const float* __restrict__ q, const float* __restrict__ k,
@@ -97,57 +128,59 @@ landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
     src = q + (off * H + (int64_t)(r - 1) * t) * d;
     dst32 = s.q_tilde + ((g * H + (r - 1)) * m) * (int64_t)d;
   }
-  double* dst64 = ws + (gi * (1 + H) + r) * (int64_t)m * d;
+  // The f64-accurate means go to the workspace as (hi, lo) pairs.
+  float2* dst2 = reinterpret_cast<float2*>(ws) + (gi * (1 + H) + r) * (int64_t)m * d;
 
   for (int i = warp; i < m_eff; i += kWarps) {
     const int lo = (int)(((int64_t)i * t) / m_eff);
     const int hi = (int)(((int64_t)(i + 1) * t) / m_eff);
-    const double inv = 1.0 / (double)(hi - lo);
+    const float nf = (float)(hi - lo);
     for (int c4 = lane; c4 < d4; c4 += 32) {
       const float* col = src + 4 * c4;
-      double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
-      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      float ah[4] = {0.f, 0.f, 0.f, 0.f}, al[4] = {0.f, 0.f, 0.f, 0.f};
       int j = lo;
       for (; j + 8 <= hi; j += 8) {
-        float x0[8], x1[8], x2[8], x3[8];
+        float x[4][8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 x = ld4(col + (int64_t)(j + u) * d);
-          x0[u] = x.x;
-          x1[u] = x.y;
-          x2[u] = x.z;
-          x3[u] = x.w;
+          const float4 v4 = ld4(col + (int64_t)(j + u) * d);
+          x[0][u] = v4.x;
+          x[1][u] = v4.y;
+          x[2][u] = v4.z;
+          x[3][u] = v4.w;
         }
-        float h, e;
-        sum8(x0, h, e);
-        a0 += (double)h;
-        l0 += e;
-        sum8(x1, h, e);
-        a1 += (double)h;
-        l1 += e;
-        sum8(x2, h, e);
-        a2 += (double)h;
-        l2 += e;
-        sum8(x3, h, e);
-        a3 += (double)h;
-        l3 += e;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float h, e;
+          sum8(x[c], h, e);
+          df_add(ah[c], al[c], h, e, ah[c], al[c]);
+        }
       }
       for (; j < hi; ++j) {
-        const float4 x = ld4(col + (int64_t)j * d);
-        a0 += (double)x.x;
-        a1 += (double)x.y;
-        a2 += (double)x.z;
-        a3 += (double)x.w;
+        const float4 v4 = ld4(col + (int64_t)j * d);
+        df_add(ah[0], al[0], v4.x, 0.f, ah[0], al[0]);
+        df_add(ah[1], al[1], v4.y, 0.f, ah[1], al[1]);
+        df_add(ah[2], al[2], v4.z, 0.f, ah[2], al[2]);
+        df_add(ah[3], al[3], v4.w, 0.f, ah[3], al[3]);
       }
-      const double m0 = (a0 + (double)l0) * inv, m1 = (a1 + (double)l1) * inv;
-      const double m2 = (a2 + (double)l2) * inv, m3 = (a3 + (double)l3) * inv;
-      double* o64 = dst64 + (int64_t)i * d + 4 * c4;
-      o64[0] = m0;
-      o64[1] = m1;
-      o64[2] = m2;
-      o64[3] = m3;
+      // The mean as a pair: q = sum / n, the exact remainder by FMA.
+      float2 mp[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float qh = ah[c] / nf;
+        const float r = fmaf(-qh, nf, ah[c]) + al[c];
+        float h, l;
+        df_fast_two_sum(qh, r / nf, h, l);
+        mp[c] = make_float2(h, l);
+      }
+      float2* o2 = dst2 + (int64_t)i * d + 4 * c4;
+      o2[0] = mp[0];
+      o2[1] = mp[1];
+      o2[2] = mp[2];
+      o2[3] = mp[3];
       float* o32 = dst32 + (int64_t)i * d + 4 * c4;
-      st4(o32, make_float4((float)m0, (float)m1, (float)m2, (float)m3));
+      st4(o32, make_float4(mp[0].x + mp[0].y, mp[1].x + mp[1].y, mp[2].x + mp[2].y,
+                           mp[3].x + mp[3].y));
     }
   }
 
@@ -189,34 +222,6 @@ landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
 // ---------------------------------------------------------------- 2
 constexpr int kTile = 32;        // landmark-product column tile
 constexpr int kTileStride = 33;  // padded row stride of the tiles (doubles)
-
-// ---- double-float arithmetic (unevaluated pairs hi + lo of f32) for the
-// f64-bound parts of the ridge pinv: GB300's f32 pipe is tens of times
-// faster than its f64 pipe.
-__device__ __forceinline__ void df_two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float z = s - a;
-  e = (a - (s - z)) + (b - z);
-}
-__device__ __forceinline__ void df_fast_two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  e = b - (s - a);
-}
-__device__ __forceinline__ void df_mul(float ah, float al, float bh, float bl, float& ph,
-                                       float& pl) {
-  const float p = ah * bh;
-  float e = fmaf(ah, bh, -p);
-  e = fmaf(ah, bl, e);
-  e = fmaf(al, bh, e);
-  df_fast_two_sum(p, e, ph, pl);
-}
-__device__ __forceinline__ void df_add(float ah, float al, float bh, float bl, float& sh,
-                                       float& sl) {
-  float s, e;
-  df_two_sum(ah, bh, s, e);
-  e += al + bl;
-  df_fast_two_sum(s, e, sh, sl);
-}
 
 // exp(xh + xl) as a double, |x| <= 700, in double-float arithmetic.
 // Cody and Waite's range reduction x = k ln2 + r with ln2 split in three
@@ -292,8 +297,9 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   float* Ql = Qh + me * kTileStride;
   float* Kh = Ql + me * kTileStride;
   float* Kl = Kh + me * kTileStride;
-  const double* K64 = ws + (gi * (1 + H)) * (int64_t)m * d;
-  const double* Q64 = ws + (gi * (1 + H) + 1 + h) * (int64_t)m * d;
+  // The landmark means as (hi, lo) pairs (landmarks_kernel).
+  const float2* K2 = reinterpret_cast<const float2*>(ws) + (gi * (1 + H)) * (int64_t)m * d;
+  const float2* Q2 = reinterpret_cast<const float2*>(ws) + (gi * (1 + H) + 1 + h) * (int64_t)m * d;
   const double scale = (double)s.scale;
 
   // A[i][j] = exp((q~64_i . k~64_j) * scale).  The dot product runs in
@@ -313,13 +319,12 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     const int cw = min(kTile, d - c0);
     for (int idx = tid; idx < me * kTile; idx += kThreads) {
       const int i = idx / kTile, cc = idx - i * kTile;
-      const double q = cc < cw ? Q64[(int64_t)i * d + c0 + cc] : 0.0;
-      const double kk = cc < cw ? K64[(int64_t)i * d + c0 + cc] : 0.0;
-      const float qh = (float)q, kh = (float)kk;
-      Qh[i * kTileStride + cc] = qh;
-      Ql[i * kTileStride + cc] = (float)(q - (double)qh);
-      Kh[i * kTileStride + cc] = kh;
-      Kl[i * kTileStride + cc] = (float)(kk - (double)kh);
+      const float2 qv = cc < cw ? Q2[(int64_t)i * d + c0 + cc] : make_float2(0.f, 0.f);
+      const float2 kv = cc < cw ? K2[(int64_t)i * d + c0 + cc] : make_float2(0.f, 0.f);
+      Qh[i * kTileStride + cc] = qv.x;
+      Ql[i * kTileStride + cc] = qv.y;
+      Kh[i * kTileStride + cc] = kv.x;
+      Kl[i * kTileStride + cc] = kv.y;
     }
     __syncthreads();
 #pragma unroll
