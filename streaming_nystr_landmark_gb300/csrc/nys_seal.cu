@@ -402,10 +402,15 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
     if (tid == 0) fail = 0;
     __syncthreads();
+    // Right-looking form of the page's Cholesky: before column j, the lower
+    // triangle right of it holds G - sum_{k<j} L_.k L_.k^T with each product
+    // subtracted in the order k = 0, 1, ... -- the same operations in the
+    // same order as the page's left-looking loop, so the same values, but
+    // each column is one parallel update instead of j-term serial sums.
+    const int cwp = tid >> 5, cln = tid & 31;
     for (int j = 0; j < me; ++j) {
       if (tid == 0) {
-        double sp = Lf[j * me + j];
-        for (int kk = 0; kk < j; ++kk) sp -= Lf[j * me + kk] * Lf[j * me + kk];
+        const double sp = Lf[j * me + j];
         if (!(sp > 0.0) || !isfinite(sp)) {
           fail = 1;
         } else {
@@ -415,10 +420,11 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
       __syncthreads();
       if (fail) break;
-      for (int i = j + 1 + tid; i < me; i += kThreads) {
-        double a = Lf[i * me + j];
-        for (int kk = 0; kk < j; ++kk) a -= Lf[i * me + kk] * Lf[j * me + kk];
-        Lf[i * me + j] = a * rdiag[j];
+      for (int i = j + 1 + tid; i < me; i += kThreads) Lf[i * me + j] *= rdiag[j];
+      __syncthreads();
+      for (int a = j + 1 + cwp; a < me; a += kThreads / 32) {
+        const double laj = Lf[a * me + j];
+        for (int b = j + 1 + cln; b <= a; b += 32) Lf[a * me + b] -= laj * Lf[b * me + j];
       }
       __syncthreads();
     }
