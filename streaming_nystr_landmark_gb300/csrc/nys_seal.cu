@@ -568,15 +568,17 @@ __device__ __forceinline__ void load_rows(const float* p, float (&a)[TR]) {
 template <int TR>
 __global__ void __launch_bounds__(kThreads, 2)
 replay_kernel(DevState s, int64_t g0, SealGeom sg,
-              const float* __restrict__ k, const float* __restrict__ v, int skip_long) {
+              const float* __restrict__ k, const float* __restrict__ v, int skip_long,
+              int heads_per_cta, int ctas_per_group) {
   constexpr int RT = 16 * TR;
   extern __shared__ __align__(16) float fsm[];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int H = s.heads, m = s.m, d = s.d, dv = s.dv, w = s.w, ns = s.sink;
   const int d4 = d >> 2;
-  const int64_t gi = blockIdx.x / H, g = g0 + gi;
-  const int h = (int)(blockIdx.x - gi * H);
-  const int64_t hb = g * H + h;
+  // Rows of this CTA: landmark r % m of head h0 + r / m (several heads of a
+  // group share the key and value blocks).
+  const int64_t gi = blockIdx.x / ctas_per_group, g = g0 + gi;
+  const int h0 = (int)(blockIdx.x - gi * ctas_per_group) * heads_per_cta;
   int t, me;
   int64_t off;
   seal_geom(sg, gi, t, me, off);
@@ -584,15 +586,16 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   const int c0 = blockIdx.y * kValTile;
   const int cw = min(kValTile, dv - c0);
   const float scale = s.scale;
-  float* QT = fsm;                     // [d][RT]   Q~ transposed, rows >= m_eff zero
+  float* QT = fsm;                     // [d][RT]   Q~ transposed, unused rows zero
   float* KT = QT + (size_t)d * RT;     // [d][kKtStride]  key block transposed
   float* PT = KT;                      // [RT][kPtStride] p, after the logits
   float* VB = KT + replay_kt_floats(RT, d);  // [kKeyBlock][kValTile]
 
-  const float* qsrc = s.q_tilde + hb * m * (int64_t)d;
   for (int idx = tid; idx < RT * d; idx += kThreads) {
     const int i = idx / d, c = idx - i * d;
-    QT[c * RT + i] = i < me ? qsrc[(int64_t)i * d + c] : 0.f;
+    const int hh = h0 + i / m, li = i - (i / m) * m;
+    const bool used = i < heads_per_cta * m && hh < H && li < me;
+    QT[c * RT + i] = used ? s.q_tilde[((g * H + hh) * (int64_t)m + li) * d + c] : 0.f;
   }
 
   float hi[TR][8], lo[TR][8], mrow[TR], zh[TR], zl[TR];
@@ -742,14 +745,16 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
 #pragma unroll
   for (int i = 0; i < TR; ++i) {
     const int row = ty * TR + i;
-    if (row >= me) continue;
+    const int hh = h0 + row / m, li = row - (row / m) * m;
+    if (row >= heads_per_cta * m || hh >= H || li >= me) continue;
+    const int64_t grow = (g * H + hh) * (int64_t)m + li;
     if (blockIdx.y == 0 && tx == 0) {
-      s.m_max[hb * m + row] = mrow[i];
-      s.z_hat[hb * m + row] = zh[i];
-      s.z_lo[hb * m + row] = zl[i];
+      s.m_max[grow] = mrow[i];
+      s.z_hat[grow] = zh[i];
+      s.z_lo[grow] = zl[i];
     }
-    float* tdst = s.t_hat + (hb * m + row) * (int64_t)dv + c0;
-    uint16_t* ldst = s.t_lo + (hb * m + row) * (int64_t)dv + c0;
+    float* tdst = s.t_hat + grow * (int64_t)dv + c0;
+    uint16_t* ldst = s.t_lo + grow * (int64_t)dv + c0;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int col = (c < 4 ? 0 : kValTile / 2 - 4) + tx * 4 + c;
@@ -761,6 +766,13 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   }
 }
 
+// Heads of a group per CUDA-core replay CTA: as many as fit in 64 landmark
+// rows (the key and value blocks are loaded once for all of them).
+inline int replay_heads_per_cta(const DevState& s) {
+  const int fit = 64 / s.m;
+  return fit < 1 ? 1 : (fit < s.heads ? fit : s.heads);
+}
+
 template <int TR>
 cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
                           const float* k, const float* v, int skip_long, cudaStream_t stream) {
@@ -768,8 +780,10 @@ cudaError_t launch_replay(const DevState& s, int64_t g0, int64_t n, const SealGe
   cudaError_t e = ensure_smem<replay_kernel<TR>>(bytes);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((s.dv + kValTile - 1) / kValTile);
-  replay_kernel<TR><<<dim3((unsigned)(n * s.heads), tiles), kThreads, bytes, stream>>>(
-      s, g0, sg, k, v, skip_long);
+  const int hpc = replay_heads_per_cta(s);
+  const int cpg = (s.heads + hpc - 1) / hpc;
+  replay_kernel<TR><<<dim3((unsigned)(n * cpg), tiles), kThreads, bytes, stream>>>(
+      s, g0, sg, k, v, skip_long, hpc, cpg);
   return cudaGetLastError();
 }
 
@@ -805,8 +819,9 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
     if (uniform) return cudaSuccess;
   }
   const int skip_long = tc ? 1 : 0;
-  if (max_me <= 16) return launch_replay<1>(s, g0, n, sg, k, v, skip_long, stream);
-  if (max_me <= 32) return launch_replay<2>(s, g0, n, sg, k, v, skip_long, stream);
+  const int rows = replay_heads_per_cta(s) * s.m;  // landmark rows per CTA
+  if (rows <= 16) return launch_replay<1>(s, g0, n, sg, k, v, skip_long, stream);
+  if (rows <= 32) return launch_replay<2>(s, g0, n, sg, k, v, skip_long, stream);
   return launch_replay<4>(s, g0, n, sg, k, v, skip_long, stream);
 }
 
