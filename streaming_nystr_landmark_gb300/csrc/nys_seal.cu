@@ -221,7 +221,7 @@ landmarks_kernel(DevState s, int64_t g0, SealGeom sg,
 
 // ---------------------------------------------------------------- 2
 constexpr int kTile = 32;        // landmark-product column tile
-constexpr int kTileStride = 33;  // padded row stride of the tiles (doubles)
+constexpr int kTileStride = 36;  // row stride of the tiles (floats): 16-byte rows
 
 // exp(xh + xl) as a double, |x| <= 700, in double-float arithmetic.
 // Cody and Waite's range reduction x = k ln2 + r with ln2 split in three
@@ -267,14 +267,12 @@ __device__ double df_exp(float xh, float xl) {
 }
 
 // Shared memory of the pinv kernel: A (later, transposed in place, the
-// right-hand sides and the solution) and the Cholesky region (first the
-// logit tiles).  About 67 KB at m = 64, so three CTAs share an SM.
-__host__ __device__ inline size_t pinv_lf_doubles(int me) {
-  const size_t a = (size_t)me * me, b = 2 * (size_t)me * kTileStride;
-  return a > b ? a : b;
-}
+// right-hand sides and the solution) and the Cholesky region, both me x me
+// doubles; before A exists the same bytes hold the four logit tiles.  64 KB
+// at m = 64, so three CTAs share an SM.
 __host__ __device__ inline size_t pinv_smem_doubles(int me) {
-  return (size_t)me * me + pinv_lf_doubles(me);
+  const size_t a = 2 * (size_t)me * me, b = 2 * (size_t)me * kTileStride;
+  return a > b ? a : b;
 }
 
 __global__ void __launch_bounds__(kThreads, 4)
@@ -292,8 +290,9 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   seal_geom(sg, gi, t_unused, me, off_unused);
   double* A = dsm;                          // [me][me]
   double* Lf = A + me * me;                 // [me][me]  A^T A + lambda I -> Cholesky factor
-  // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x).
-  float* Qh = reinterpret_cast<float*>(Lf);  // [me][kTileStride] each, before Lf is used
+  // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x), in the
+  // bytes of A and Lf before either is written.
+  float* Qh = reinterpret_cast<float*>(dsm);  // [me][kTileStride] each
   float* Ql = Qh + me * kTileStride;
   float* Kh = Ql + me * kTileStride;
   float* Kl = Kh + me * kTileStride;
@@ -308,7 +307,14 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   // terms hi*lo + lo*hi into its error, Knuth two-sum into an unevaluated
   // (sh, sl) pair.  Relative to sum|q_c k_c| the result is within ~1e-13 of
   // the f64 dot product; exp and everything after run in f64.
+  // Thread tid < R*me (R = kThreads / me rows per pass) owns column
+  // j = tid % me and rows i0 + p*R; key and query rows are read as float4
+  // pairs (the query row is the same for the whole warp when me divides 256,
+  // a broadcast).  Tile columns past d are zero and add exactly nothing.
   constexpr int kPer = (kMaxM * kMaxM + kThreads - 1) / kThreads;
+  const int R = kThreads / me;
+  const bool lact = tid < R * me;
+  const int lj = lact ? tid % me : 0, li0 = lact ? tid / me : me;
   float sh[kPer], sl[kPer];
 #pragma unroll
   for (int p = 0; p < kPer; ++p) {
@@ -327,41 +333,50 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       Kl[i * kTileStride + cc] = kv.y;
     }
     __syncthreads();
+    if (lact) {
+      const float4* kh4 = reinterpret_cast<const float4*>(Kh + lj * kTileStride);
+      const float4* kl4 = reinterpret_cast<const float4*>(Kl + lj * kTileStride);
 #pragma unroll
-    for (int p = 0; p < kPer; ++p) {
-      const int pair = tid + p * kThreads;
-      if (pair < me * me) {
-        const int i = pair / me, j = pair - i * me;
-        const float* qh = Qh + i * kTileStride;
-        const float* ql = Ql + i * kTileStride;
-        const float* kh = Kh + j * kTileStride;
-        const float* kl = Kl + j * kTileStride;
-        float a = sh[p], b = sl[p];
-        for (int cc = 0; cc < cw; ++cc) {
-          const float pr = qh[cc] * kh[cc];
-          float pe = fmaf(qh[cc], kh[cc], -pr);
-          pe = fmaf(qh[cc], kl[cc], fmaf(ql[cc], kh[cc], pe));
-          const float t = a + pr;
-          const float z = t - a;
-          b += ((a - (t - z)) + (pr - z)) + pe;
-          a = t;
+      for (int p = 0; p < kPer; ++p) {
+        const int i = li0 + p * R;
+        if (i < me) {
+          const float4* qh4 = reinterpret_cast<const float4*>(Qh + i * kTileStride);
+          const float4* ql4 = reinterpret_cast<const float4*>(Ql + i * kTileStride);
+          float a = sh[p], b = sl[p];
+          auto term = [&](float x, float xl, float y, float yl) {
+            const float pr = x * y;
+            float pe = fmaf(x, y, -pr);
+            pe = fmaf(x, yl, fmaf(xl, y, pe));
+            const float t = a + pr;
+            const float z = t - a;
+            b += ((a - (t - z)) + (pr - z)) + pe;
+            a = t;
+          };
+#pragma unroll 2
+          for (int c4 = 0; c4 < kTile / 4; ++c4) {
+            const float4 qh = qh4[c4], ql = ql4[c4], kh = kh4[c4], kl = kl4[c4];
+            term(qh.x, ql.x, kh.x, kl.x);
+            term(qh.y, ql.y, kh.y, kl.y);
+            term(qh.z, ql.z, kh.z, kl.z);
+            term(qh.w, ql.w, kh.w, kl.w);
+          }
+          sh[p] = a;
+          sl[p] = b;
         }
-        sh[p] = a;
-        sl[p] = b;
       }
     }
     __syncthreads();
   }
 #pragma unroll
   for (int p = 0; p < kPer; ++p) {
-    const int pair = tid + p * kThreads;
-    if (pair < me * me) {
+    const int i = li0 + p * R;
+    if (i < me) {
       // logit * scale as a pair (scale is an f32 value), exp in double-float;
       // non-finite or huge logits keep the f64 exp's semantics.
       float xh, xl;
       df_mul(sh[p], sl[p], (float)scale, 0.f, xh, xl);
-      A[pair] = (fabsf(xh) <= 700.f) ? df_exp(xh, xl)
-                                      : exp(((double)sh[p] + (double)sl[p]) * scale);
+      A[i * me + lj] = (fabsf(xh) <= 700.f) ? df_exp(xh, xl)
+                                             : exp(((double)sh[p] + (double)sl[p]) * scale);
     }
   }
   __syncthreads();
@@ -479,19 +494,27 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       df_add(w.x, w.y, -ph, -pl, nh, nl);
       W[i * me + j] = make_float2(nh, nl);
     };
+    // y = W_kj / L_kk once per pivot and column: row k is final at pivot k.
+    constexpr int kCols = (kMaxM + 31) / 32;
+    float yh[kCols], yl[kCols];
+    auto pivot_row = [&](int k) {
+#pragma unroll
+      for (int c = 0; c < kCols; ++c)
+        if (lan + 32 * c < me) scaled(k, lan + 32 * c, yh[c], yl[c]);
+    };
+    constexpr int kWarps = kThreads / 32;
     for (int k = 0; k < me - 1; ++k) {  // forward: rows below the pivot
-      for (int i = wrp; i < me; i += kThreads / 32) {
-        if (i <= k) continue;
+      pivot_row(k);
+      const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kWarps + 1) * kWarps;
+      for (int i = i0; i < me; i += kWarps) {
         const float2 lik = L2[i * me + k];
-        for (int j = lan; j < me; j += 32) {
-          float yh, yl;
-          scaled(k, j, yh, yl);
-          update(i, j, lik, yh, yl);
-        }
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (lan + 32 * c < me) update(i, lan + 32 * c, lik, yh[c], yl[c]);
       }
       __syncthreads();
     }
-    for (int i = wrp; i < me; i += kThreads / 32)  // Y = W / diag(L)
+    for (int i = wrp; i < me; i += kWarps)  // Y = W / diag(L)
       for (int j = lan; j < me; j += 32) {
         float h, l;
         scaled(i, j, h, l);
@@ -499,13 +522,12 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
     __syncthreads();
     for (int k = me - 1; k > 0; --k) {  // backward: rows above the pivot
-      for (int i = wrp; i < k; i += kThreads / 32) {
+      pivot_row(k);
+      for (int i = wrp; i < k; i += kWarps) {
         const float2 lki = L2[k * me + i];  // (L^T)_ik = L_ki
-        for (int j = lan; j < me; j += 32) {
-          float xh, xl;
-          scaled(k, j, xh, xl);
-          update(i, j, lki, xh, xl);
-        }
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (lan + 32 * c < me) update(i, lan + 32 * c, lki, yh[c], yl[c]);
       }
       __syncthreads();
     }
