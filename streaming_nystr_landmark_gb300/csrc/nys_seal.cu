@@ -275,12 +275,13 @@ __host__ __device__ inline size_t pinv_smem_doubles(int me) {
   return a > b ? a : b;
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+template <int NT, int MM>
+__global__ void __launch_bounds__(NT, 1024 / NT)
 pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) {
   extern __shared__ __align__(16) double dsm[];
   __shared__ int fail;
   __shared__ double lam_s, mean_diag_s;
-  __shared__ double rdiag[kMaxM];  // 1 / L_jj: one f64 division per column
+  __shared__ double rdiag[MM];  // 1 / L_jj: one f64 division per column
   const int tid = threadIdx.x;
   const int H = s.heads, m = s.m, d = s.d;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
@@ -307,12 +308,12 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   // terms hi*lo + lo*hi into its error, Knuth two-sum into an unevaluated
   // (sh, sl) pair.  Relative to sum|q_c k_c| the result is within ~1e-13 of
   // the f64 dot product; exp and everything after run in f64.
-  // Thread tid < R*me (R = kThreads / me rows per pass) owns column
+  // Thread tid < R*me (R = NT / me rows per pass) owns column
   // j = tid % me and rows i0 + p*R; key and query rows are read as float4
   // pairs (the query row is the same for the whole warp when me divides 256,
   // a broadcast).  Tile columns past d are zero and add exactly nothing.
-  constexpr int kPer = (kMaxM * kMaxM + kThreads - 1) / kThreads;
-  const int R = kThreads / me;
+  constexpr int kPer = (MM * MM + NT - 1) / NT;
+  const int R = NT / me;
   const bool lact = tid < R * me;
   const int lj = lact ? tid % me : 0, li0 = lact ? tid / me : me;
   float sh[kPer], sl[kPer];
@@ -323,7 +324,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   }
   for (int c0 = 0; c0 < d; c0 += kTile) {
     const int cw = min(kTile, d - c0);
-    for (int idx = tid; idx < me * kTile; idx += kThreads) {
+    for (int idx = tid; idx < me * kTile; idx += NT) {
       const int i = idx / kTile, cc = idx - i * kTile;
       const float2 qv = cc < cw ? Q2[(int64_t)i * d + c0 + cc] : make_float2(0.f, 0.f);
       const float2 kv = cc < cw ? K2[(int64_t)i * d + c0 + cc] : make_float2(0.f, 0.f);
@@ -387,7 +388,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   // order, so the same values).
   const int tri = me * (me + 1) / 2;
   auto build_gram = [&](double lam) {
-    for (int p = tid; p < tri; p += kThreads) {
+    for (int p = tid; p < tri; p += NT) {
       int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
       while (i * (i + 1) / 2 > p) --i;
       while ((i + 1) * (i + 2) / 2 <= p) ++i;
@@ -411,7 +412,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   for (int attempt = 0; attempt < 12 && !solved; ++attempt) {
     const double lam = lam_s;
     if (attempt == 0) {
-      for (int i = tid; i < me; i += kThreads) Lf[i * me + i] += lam;
+      for (int i = tid; i < me; i += NT) Lf[i * me + i] += lam;
     } else {
       build_gram(lam);
     }
@@ -435,9 +436,9 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
       __syncthreads();
       if (fail) break;
-      for (int i = j + 1 + tid; i < me; i += kThreads) Lf[i * me + j] *= rdiag[j];
+      for (int i = j + 1 + tid; i < me; i += NT) Lf[i * me + j] *= rdiag[j];
       __syncthreads();
-      for (int a = j + 1 + cwp; a < me; a += kThreads / 32) {
+      for (int a = j + 1 + cwp; a < me; a += NT / 32) {
         const double laj = Lf[a * me + j];
         for (int b = j + 1 + cln; b <= a; b += 32) Lf[a * me + b] -= laj * Lf[b * me + j];
       }
@@ -463,9 +464,9 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     // A (transposed there).
     float2* L2 = reinterpret_cast<float2*>(Lf);
     float2* W = reinterpret_cast<float2*>(A);
-    __shared__ float2 rd2[kMaxM];
+    __shared__ float2 rd2[MM];
     __syncthreads();
-    for (int e = tid; e < me * me; e += kThreads) {
+    for (int e = tid; e < me * me; e += NT) {
       const int i = e / me, j = e - i * me;
       const double l = Lf[e];  // read, then overwritten by its own pair
       L2[e] = make_float2((float)l, (float)(l - (double)(float)l));
@@ -475,7 +476,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
         W[j * me + i] = make_float2((float)aij, (float)(aij - (double)(float)aij));
       }
     }
-    for (int k = tid; k < me; k += kThreads) {
+    for (int k = tid; k < me; k += NT) {
       const double r = rdiag[k];
       rd2[k] = make_float2((float)r, (float)(r - (double)(float)r));
     }
@@ -495,14 +496,14 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       W[i * me + j] = make_float2(nh, nl);
     };
     // y = W_kj / L_kk once per pivot and column: row k is final at pivot k.
-    constexpr int kCols = (kMaxM + 31) / 32;
+    constexpr int kCols = (MM + 31) / 32;
     float yh[kCols], yl[kCols];
     auto pivot_row = [&](int k) {
 #pragma unroll
       for (int c = 0; c < kCols; ++c)
         if (lan + 32 * c < me) scaled(k, lan + 32 * c, yh[c], yl[c]);
     };
-    constexpr int kWarps = kThreads / 32;
+    constexpr int kWarps = NT / 32;
     for (int k = 0; k < me - 1; ++k) {  // forward: rows below the pivot
       pivot_row(k);
       const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kWarps + 1) * kWarps;
@@ -531,7 +532,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
       __syncthreads();
     }
-    for (int pair = tid; pair < me * me; pair += kThreads) {  // M = W / diag(L)
+    for (int pair = tid; pair < me * me; pair += NT) {  // M = W / diag(L)
       const int i = pair / me, j = pair - i * me;
       float h, l;
       scaled(i, j, h, l);
@@ -539,7 +540,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
   } else {
     const double diag = 1.0 / fmax(mean_diag_s, DBL_MIN);
-    for (int pair = tid; pair < me * me; pair += kThreads) {
+    for (int pair = tid; pair < me * me; pair += NT) {
       const int i = pair / me, j = pair - i * me;
       M[i * m + j] = (i == j) ? (float)diag : 0.f;
     }
@@ -824,9 +825,17 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
                                                                             ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+  // Up to 32 landmarks: 128-thread CTAs, eight per SM, so that the serial
+  // steps of one head's Cholesky overlap with more heads' parallel work.
   const size_t pbytes = pinv_smem_doubles(max_me) * sizeof(double);
-  if ((e = ensure_smem<pinv_kernel>(pbytes)) != cudaSuccess) return e;
-  pinv_kernel<<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(s, g0, sg, ws);
+  if (max_me <= 32) {
+    if ((e = ensure_smem<pinv_kernel<128, 32>>(pbytes)) != cudaSuccess) return e;
+    pinv_kernel<128, 32><<<(unsigned)(n * s.heads), 128, pbytes, stream>>>(s, g0, sg, ws);
+  } else {
+    if ((e = ensure_smem<pinv_kernel<kThreads, kMaxM>>(pbytes)) != cudaSuccess) return e;
+    pinv_kernel<kThreads, kMaxM><<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(
+        s, g0, sg, ws);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // Replay: tensor cores for groups with long prompts (where the geometry
