@@ -266,14 +266,18 @@ __device__ double df_exp(float xh, float xl) {
   return ldexp((double)sh + (double)sl, (int)k);
 }
 
-// Shared memory of the pinv kernel: A (later, transposed in place, the
-// right-hand sides and the solution) and the Cholesky region, both me x me
-// doubles; before A exists the same bytes hold the four logit tiles.  64 KB
-// at m = 64, so three CTAs share an SM.
+// Shared memory of the pinv kernel: A (me x me doubles; later, transposed in
+// place, the right-hand sides and the solution) and the lower triangle of the
+// Cholesky region, packed row by row (me (me + 1) / 2 doubles); before A
+// exists the same bytes hold the four logit tiles.  49 KB at m = 64, so four
+// CTAs share an SM.
 __host__ __device__ inline size_t pinv_smem_doubles(int me) {
-  const size_t a = 2 * (size_t)me * me, b = 2 * (size_t)me * kTileStride;
+  const size_t a = (size_t)me * me + (size_t)me * (me + 1) / 2;
+  const size_t b = 2 * (size_t)me * kTileStride;
   return a > b ? a : b;
 }
+// Packed index of (i, j), j <= i, in a lower triangle stored row by row.
+__device__ __forceinline__ int tri_idx(int i, int j) { return i * (i + 1) / 2 + j; }
 
 template <int NT, int MM>
 __global__ void __launch_bounds__(NT, 1024 / NT)
@@ -282,6 +286,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   __shared__ int fail;
   __shared__ double lam_s, mean_diag_s;
   __shared__ double rdiag[MM];  // 1 / L_jj: one f64 division per column
+  __shared__ double colj[MM];   // the current Cholesky column, L_ij for i > j
   const int tid = threadIdx.x;
   const int H = s.heads, m = s.m, d = s.d;
   const int64_t gi = blockIdx.x / H, g = g0 + gi;
@@ -290,7 +295,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   int64_t off_unused;
   seal_geom(sg, gi, t_unused, me, off_unused);
   double* A = dsm;                          // [me][me]
-  double* Lf = A + me * me;                 // [me][me]  A^T A + lambda I -> Cholesky factor
+  double* Lf = A + me * me;  // packed lower triangle: A^T A + lambda I -> Cholesky factor
   // Landmark tiles as f32 pairs x = hi + lo (exact to ~2^-48 of x), in the
   // bytes of A and Lf before either is written.
   float* Qh = reinterpret_cast<float*>(dsm);  // [me][kTileStride] each
@@ -395,14 +400,14 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       const int j = p - i * (i + 1) / 2;
       double a = 0.0;
       for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
-      Lf[i * me + j] = (i == j) ? a + lam : a;
+      Lf[p] = (i == j) ? a + lam : a;  // p = tri_idx(i, j)
     }
   };
   build_gram(0.0);
   __syncthreads();
   if (tid == 0) {
     double sd = 0.0;
-    for (int i = 0; i < me; ++i) sd += Lf[i * me + i];
+    for (int i = 0; i < me; ++i) sd += Lf[tri_idx(i, i)];
     mean_diag_s = sd / (double)me;
     lam_s = 1e-6 * fmax(mean_diag_s, DBL_MIN);
   }
@@ -412,7 +417,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
   for (int attempt = 0; attempt < 12 && !solved; ++attempt) {
     const double lam = lam_s;
     if (attempt == 0) {
-      for (int i = tid; i < me; i += NT) Lf[i * me + i] += lam;
+      for (int i = tid; i < me; i += NT) Lf[tri_idx(i, i)] += lam;
     } else {
       build_gram(lam);
     }
@@ -423,24 +428,31 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     // subtracted in the order k = 0, 1, ... -- the same operations in the
     // same order as the page's left-looking loop, so the same values, but
     // each column is one parallel update instead of j-term serial sums.
+    // The scaled column is also copied to colj, so the update reads it
+    // without bank conflicts.
     const int cwp = tid >> 5, cln = tid & 31;
     for (int j = 0; j < me; ++j) {
       if (tid == 0) {
-        const double sp = Lf[j * me + j];
+        const double sp = Lf[tri_idx(j, j)];
         if (!(sp > 0.0) || !isfinite(sp)) {
           fail = 1;
         } else {
-          Lf[j * me + j] = sqrt(sp);
-          rdiag[j] = 1.0 / Lf[j * me + j];
+          Lf[tri_idx(j, j)] = sqrt(sp);
+          rdiag[j] = 1.0 / Lf[tri_idx(j, j)];
         }
       }
       __syncthreads();
       if (fail) break;
-      for (int i = j + 1 + tid; i < me; i += NT) Lf[i * me + j] *= rdiag[j];
+      for (int i = j + 1 + tid; i < me; i += NT) {
+        const double lij = Lf[tri_idx(i, j)] * rdiag[j];
+        Lf[tri_idx(i, j)] = lij;
+        colj[i] = lij;
+      }
       __syncthreads();
       for (int a = j + 1 + cwp; a < me; a += NT / 32) {
-        const double laj = Lf[a * me + j];
-        for (int b = j + 1 + cln; b <= a; b += 32) Lf[a * me + b] -= laj * Lf[b * me + j];
+        const double laj = colj[a];
+        double* row = Lf + tri_idx(a, 0);
+        for (int b = j + 1 + cln; b <= a; b += 32) row[b] -= laj * colj[b];
       }
       __syncthreads();
     }
@@ -466,10 +478,12 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     float2* W = reinterpret_cast<float2*>(A);
     __shared__ float2 rd2[MM];
     __syncthreads();
-    for (int e = tid; e < me * me; e += NT) {
-      const int i = e / me, j = e - i * me;
+    for (int e = tid; e < tri; e += NT) {
       const double l = Lf[e];  // read, then overwritten by its own pair
       L2[e] = make_float2((float)l, (float)(l - (double)(float)l));
+    }
+    for (int e = tid; e < me * me; e += NT) {
+      const int i = e / me, j = e - i * me;
       if (i <= j) {  // W[i][j] = A^T[i][j] = A[j][i]: swap the pair (i, j), (j, i)
         const double aij = A[i * me + j], aji = A[j * me + i];
         W[i * me + j] = make_float2((float)aji, (float)(aji - (double)(float)aji));
@@ -508,7 +522,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       pivot_row(k);
       const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kWarps + 1) * kWarps;
       for (int i = i0; i < me; i += kWarps) {
-        const float2 lik = L2[i * me + k];
+        const float2 lik = L2[tri_idx(i, k)];
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
           if (lan + 32 * c < me) update(i, lan + 32 * c, lik, yh[c], yl[c]);
@@ -525,7 +539,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     for (int k = me - 1; k > 0; --k) {  // backward: rows above the pivot
       pivot_row(k);
       for (int i = wrp; i < k; i += kWarps) {
-        const float2 lki = L2[k * me + i];  // (L^T)_ik = L_ki
+        const float2 lki = L2[tri_idx(k, i)];  // (L^T)_ik = L_ki
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
           if (lan + 32 * c < me) update(i, lan + 32 * c, lki, yh[c], yl[c]);
