@@ -586,7 +586,7 @@ __host__ __device__ inline size_t replay_kt_floats(int rt, int d) {
   return a > b ? a : b;
 }
 __host__ __device__ inline size_t replay_smem_floats(int rt, int d) {
-  return (size_t)d * rt + replay_kt_floats(rt, d) + (size_t)kKeyBlock * kValTile;
+  return (size_t)d * (rt + 4) + replay_kt_floats(rt, d) + (size_t)kKeyBlock * kValTile;
 }
 
 template <int TR>
@@ -623,16 +623,50 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   const int c0 = blockIdx.y * kValTile;
   const int cw = min(kValTile, dv - c0);
   const float scale = s.scale;
-  float* QT = fsm;                     // [d][RT]   Q~ transposed, unused rows zero
-  float* KT = QT + (size_t)d * RT;     // [d][kKtStride]  key block transposed
+  constexpr int QTS = RT + 4;          // row stride of QT: conflict-free transposed stores
+  float* QT = fsm;                     // [d][QTS]  Q~ transposed, unused rows zero
+  float* KT = QT + (size_t)d * QTS;    // [d][kKtStride]  key block transposed
   float* PT = KT;                      // [RT][kPtStride] p, after the logits
   float* VB = KT + replay_kt_floats(RT, d);  // [kKeyBlock][kValTile]
 
-  for (int idx = tid; idx < RT * d; idx += kThreads) {
-    const int i = idx / d, c = idx - i * d;
-    const int hh = h0 + i / m, li = i - (i / m) * m;
-    const bool used = i < heads_per_cta * m && hh < H && li < me;
-    QT[c * RT + i] = used ? s.q_tilde[((g * H + hh) * (int64_t)m + li) * d + c] : 0.f;
+  // Q~ rows, transposed, moved like the key blocks below: thread
+  // (klane, kchunk) takes float4 chunks kchunk, kchunk + 16, ... of rows
+  // klane, klane + 16, ...; all of a thread's loads are issued before its
+  // stores.
+  const int klane = tid & 15, kchunk = tid >> 4;  // 16 rows x 16 chunk lanes
+  {
+    float4 qx[TR][2];
+#pragma unroll
+    for (int a = 0; a < TR; ++a) {
+      const int i = klane + 16 * a;
+      const int hh = h0 + i / m, li = i - (i / m) * m;
+      const bool used = i < heads_per_cta * m && hh < H && li < me;
+      const float* src = s.q_tilde + ((g * H + hh) * (int64_t)m + li) * d;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int c4 = kchunk + 16 * b;
+        qx[a][b] = (used && c4 < d4) ? ld4(src + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int c4 = kchunk + 32; c4 < d4; c4 += 16) {  // d > 128
+        const float4 x = used ? ld4(src + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        QT[(4 * c4 + 0) * QTS + i] = x.x;
+        QT[(4 * c4 + 1) * QTS + i] = x.y;
+        QT[(4 * c4 + 2) * QTS + i] = x.z;
+        QT[(4 * c4 + 3) * QTS + i] = x.w;
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < TR; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int i = klane + 16 * a, c4 = kchunk + 16 * b;
+        if (c4 < d4) {
+          QT[(4 * c4 + 0) * QTS + i] = qx[a][b].x;
+          QT[(4 * c4 + 1) * QTS + i] = qx[a][b].y;
+          QT[(4 * c4 + 2) * QTS + i] = qx[a][b].z;
+          QT[(4 * c4 + 3) * QTS + i] = qx[a][b].w;
+        }
+      }
   }
 
   float hi[TR][8], lo[TR][8], mrow[TR], zh[TR], zl[TR];
@@ -651,32 +685,70 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
   const float* ksrc = k + off * d;
   const float* vsrc = v + off * dv + c0;
   const int j_end = t - w;  // keys sink .. t-w-1 were evicted by the replay
-  const int klane = tid & 15, kchunk = tid >> 4;  // 16 keys x 16 chunk lanes
   for (int j0 = ns; j0 < j_end; j0 += kKeyBlock) {
     const int nb = min(kKeyBlock, j_end - j0);
     __syncthreads();  // the previous block is done with KT / PT / VB
     // Keys, transposed: thread (klane, kchunk) moves float4 chunks
-    // kchunk, kchunk + 16, ... of keys klane, klane + 16, ...
-    for (int kk = klane; kk < kKeyBlock; kk += 16) {
-      const bool valid = kk < nb;
-      const float* row = ksrc + (int64_t)(j0 + kk) * d;
-      for (int c4 = kchunk; c4 < d4; c4 += 16) {
-        const float4 x = valid ? *reinterpret_cast<const float4*>(row + 4 * c4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        KT[(4 * c4 + 0) * kKtStride + kk] = x.x;
-        KT[(4 * c4 + 1) * kKtStride + kk] = x.y;
-        KT[(4 * c4 + 2) * kKtStride + kk] = x.z;
-        KT[(4 * c4 + 3) * kKtStride + kk] = x.w;
+    // kchunk, kchunk + 16, ... of keys klane, klane + 16, ...; values of
+    // this column tile (rows past the block are zero).  A thread loads its
+    // key chunks (the first two of each row), then its value chunks, each
+    // set before any of its stores.
+    {
+      constexpr int kKR = kKeyBlock / 16;                  // key rows per thread
+      constexpr int kVR = kKeyBlock * (kValTile / 4) / kThreads;  // value chunks per thread
+      const int cw4 = cw >> 2;
+#pragma unroll
+      for (int a0 = 0; a0 < kKR; a0 += 2) {  // two key rows' chunks in flight
+        float4 kx[2][2];
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const int kk = klane + 16 * (a0 + a);
+          const float* row = ksrc + (int64_t)(j0 + kk) * d;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int c4 = kchunk + 16 * b;
+            kx[a][b] =
+                (kk < nb && c4 < d4) ? ld4(row + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const int kk = klane + 16 * (a0 + a);
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int c4 = kchunk + 16 * b;
+            if (c4 < d4) {
+              KT[(4 * c4 + 0) * kKtStride + kk] = kx[a][b].x;
+              KT[(4 * c4 + 1) * kKtStride + kk] = kx[a][b].y;
+              KT[(4 * c4 + 2) * kKtStride + kk] = kx[a][b].z;
+              KT[(4 * c4 + 3) * kKtStride + kk] = kx[a][b].w;
+            }
+          }
+          const float* row = ksrc + (int64_t)(j0 + kk) * d;
+          for (int c4 = kchunk + 32; c4 < d4; c4 += 16) {  // d > 128
+            const float4 x = kk < nb ? ld4(row + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            KT[(4 * c4 + 0) * kKtStride + kk] = x.x;
+            KT[(4 * c4 + 1) * kKtStride + kk] = x.y;
+            KT[(4 * c4 + 2) * kKtStride + kk] = x.z;
+            KT[(4 * c4 + 3) * kKtStride + kk] = x.w;
+          }
+        }
       }
-    }
-    // Values of this column tile; rows past the block are zero.
-    const int cw4 = cw >> 2;
-    for (int idx = tid; idx < kKeyBlock * (kValTile / 4); idx += kThreads) {
-      const int jj = idx >> 5, c4 = idx & 31;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (jj < nb && c4 < cw4)
-        x = *reinterpret_cast<const float4*>(vsrc + (int64_t)(j0 + jj) * dv + 4 * c4);
-      *reinterpret_cast<float4*>(VB + jj * kValTile + 4 * c4) = x;
+#pragma unroll
+      for (int e0 = 0; e0 < kVR; e0 += 4) {  // four value chunks in flight
+        float4 vx[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int idx = tid + (e0 + e) * kThreads, jj = idx >> 5, c4 = idx & 31;
+          vx[e] = (jj < nb && c4 < cw4) ? ld4(vsrc + (int64_t)(j0 + jj) * dv + 4 * c4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int idx = tid + (e0 + e) * kThreads, jj = idx >> 5, c4 = idx & 31;
+          *reinterpret_cast<float4*>(VB + jj * kValTile + 4 * c4) = vx[e];
+        }
+      }
     }
     __syncthreads();
 
@@ -688,7 +760,7 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
 #pragma unroll 4
     for (int c = 0; c < d; ++c) {
       float a[TR];
-      load_rows<TR>(QT + c * RT + ty * TR, a);
+      load_rows<TR>(QT + c * QTS + ty * TR, a);
       const float4 b = *reinterpret_cast<const float4*>(KT + c * kKtStride + tx * 4);
 #pragma unroll
       for (int i = 0; i < TR; ++i) {
