@@ -373,6 +373,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
     __syncthreads();
   }
+  float xmax = -INFINITY;
 #pragma unroll
   for (int p = 0; p < kPer; ++p) {
     const int i = li0 + p * R;
@@ -383,9 +384,27 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       df_mul(sh[p], sl[p], (float)scale, 0.f, xh, xl);
       A[i * me + lj] = (fabsf(xh) <= 700.f) ? df_exp(xh, xl)
                                              : exp(((double)sh[p] + (double)sl[p]) * scale);
+      xmax = (xh == xh) ? fmaxf(xmax, xh) : INFINITY;  // NaN: take the f64 path
     }
   }
-  __syncthreads();
+  // A^T A in double-float on the fp32 pipe when every entry of A lies in
+  // [e^-41, e^41] (about 2^-59 .. 2^59): its products then stay far inside
+  // the f32 range and the pairs keep ~2^-48 of each value; A > 0, so no sum
+  // cancels and each entry is within ~2^-47 of the f64 sum, the order of
+  // that sum's own rounding.  Otherwise A^T A is summed in f64.  The logits
+  // of the maximum bound A's maximum; the entries below it need no bound
+  // (an entry under 2^-100 adds under 2^-200 m to an A^T A entry, far below
+  // the ridge lambda, which is >= 1e-6 * max_i (A^T A)_ii / m).
+  const bool below = __syncthreads_and(xmax <= 41.f), above = __syncthreads_or(xmax >= -41.f);
+  const bool df_gram = below && above;
+  float2* A2 = reinterpret_cast<float2*>(A);  // A as (hi, lo) pairs on that path
+  if (df_gram) {
+    for (int e = tid; e < me * me; e += NT) {
+      const double a = A[e];  // read, then overwritten by its own pair
+      A2[e] = make_float2((float)a, (float)(a - (double)(float)a));
+    }
+    __syncthreads();
+  }
 
   // G = A^T A + lambda I into Lf, lower triangle only (all the Cholesky
   // reads), the triangle enumerated densely so that every lane has a pair.
@@ -398,8 +417,24 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       while (i * (i + 1) / 2 > p) --i;
       while ((i + 1) * (i + 2) / 2 <= p) ++i;
       const int j = p - i * (i + 1) / 2;
-      double a = 0.0;
-      for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
+      double a;
+      if (df_gram) {
+        float gh = 0.f, gl = 0.f;
+        for (int kk = 0; kk < me; ++kk) {
+          const float2 x = A2[kk * me + i], y = A2[kk * me + j];
+          const float pr = x.x * y.x;
+          float pe = fmaf(x.x, y.x, -pr);
+          pe = fmaf(x.x, y.y, fmaf(x.y, y.x, pe));
+          const float t = gh + pr;
+          const float z = t - gh;
+          gl += ((gh - (t - z)) + (pr - z)) + pe;
+          gh = t;
+        }
+        a = (double)gh + (double)gl;
+      } else {
+        a = 0.0;
+        for (int kk = 0; kk < me; ++kk) a = fma(A[kk * me + i], A[kk * me + j], a);
+      }
       Lf[p] = (i == j) ? a + lam : a;  // p = tri_idx(i, j)
     }
   };
@@ -484,7 +519,13 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
     for (int e = tid; e < me * me; e += NT) {
       const int i = e / me, j = e - i * me;
-      if (i <= j) {  // W[i][j] = A^T[i][j] = A[j][i]: swap the pair (i, j), (j, i)
+      if (df_gram) {  // A is already in pairs: W = A^T by swapping them
+        if (i < j) {
+          const float2 aij = A2[i * me + j], aji = A2[j * me + i];
+          W[i * me + j] = aji;
+          W[j * me + i] = aij;
+        }
+      } else if (i <= j) {  // W[i][j] = A^T[i][j] = A[j][i]: swap the pair (i, j), (j, i)
         const double aij = A[i * me + j], aji = A[j * me + i];
         W[i * me + j] = make_float2((float)aji, (float)(aji - (double)(float)aji));
         W[j * me + i] = make_float2((float)aij, (float)(aij - (double)(float)aij));

@@ -1,11 +1,11 @@
 """GPU-side ABI behaviour: error codes on a live device, sub-range and empty
-launches, the non-finite ridge fallback, and the step kernel alone on a state
-uploaded from the oracle."""
+launches, the non-finite ridge fallback, large finite landmark logits, and the
+step kernel alone on a state uploaded from the oracle."""
 import numpy as np
 import pytest
 
 from oracle import NystromOracle
-from parity_util import OUT_TOL, row_err
+from parity_util import OUT_TOL, compare_group_state, read_state, row_err
 from streaming_nystr_landmark_gb300 import nys
 from streaming_nystr_landmark_gb300.workloads import (Workload, host_prompt_batch,
                                                       host_token_batch)
@@ -118,6 +118,44 @@ def test_overflowing_landmark_kernel_takes_ridge_fallback(cuda_device):
         out = torch.empty((1, 2, 32), device=cuda_device)
         st.step(*_to(cuda_device, tq[None], tk[None], tv[None]), out, g0=g, n=1)
         for h in range(2):
+            assert row_err(out[0, h].cpu().numpy().astype(np.float64), ref[h]) <= OUT_TOL
+    st.close()
+
+
+def test_large_landmark_logits_sum_gram_in_f64(cuda_device):
+    """Landmark logits of 60 (A up to e^60, finite): past the +-41 bound of
+    the double-float A^T A, so the pinv sums A^T A in f64; the sealed state
+    and a decode step still match the oracle.  Every prompt segment is
+    constant (keys and queries alpha e_b in segment b), so the landmarks are
+    alpha e_b and A = J + (e^60 - 1) I is well conditioned."""
+    import torch
+    wl, st = _small(cuda_device, groups=2)
+    t, d, m, H = wl.t, wl.d, wl.m, wl.heads_per_kv
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
+    alpha = np.float32(np.sqrt(60.0 / scale))
+    seg = np.arange(t) * m // t  # segment of each prompt position (t = 8 m)
+    rng = np.random.default_rng(11)
+    q = np.zeros((2, H, t, d), np.float32)
+    q[:, :, np.arange(t), seg] = alpha
+    k = np.zeros((2, t, d), np.float32)
+    k[:, np.arange(t), seg] = alpha
+    v = rng.standard_normal((2, t, wl.dv)).astype(np.float32)
+    st.seal(*_to(cuda_device, q, k, v))
+    torch.cuda.synchronize()
+    reg = read_state(st)
+    for g in range(2):
+        o = NystromOracle(m, wl.w, wl.sink, H)
+        o.prefill(q[g], k[g], v[g])
+        for h in range(H):
+            assert not o.hs[h].ridge.fallback
+        compare_group_state(reg, g, o)
+        tq = rng.standard_normal((H, d)).astype(np.float32)
+        tk = rng.standard_normal(d).astype(np.float32)
+        tv = rng.standard_normal(wl.dv).astype(np.float32)
+        ref = o.step(tq, tk, tv)
+        out = torch.empty((1, H, wl.dv), device=cuda_device)
+        st.step(*_to(cuda_device, tq[None], tk[None], tv[None]), out, g0=g, n=1)
+        for h in range(H):
             assert row_err(out[0, h].cpu().numpy().astype(np.float64), ref[h]) <= OUT_TOL
     st.close()
 
