@@ -464,19 +464,21 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     // same order as the page's left-looking loop, so the same values, but
     // each column is one parallel update instead of j-term serial sums.
     // The scaled column is also copied to colj, so the update reads it
-    // without bank conflicts.
+    // without bank conflicts.  The lane that updates the next diagonal entry
+    // (j+1, j+1) takes its square root and reciprocal right after, so a
+    // column costs two barriers.
     const int cwp = tid >> 5, cln = tid & 31;
-    for (int j = 0; j < me; ++j) {
-      if (tid == 0) {
-        const double sp = Lf[tri_idx(j, j)];
-        if (!(sp > 0.0) || !isfinite(sp)) {
-          fail = 1;
-        } else {
-          Lf[tri_idx(j, j)] = sqrt(sp);
-          rdiag[j] = 1.0 / Lf[tri_idx(j, j)];
-        }
+    auto pivot = [&](int j, double sp) {  // L_jj = sqrt(sp), or fail
+      if (!(sp > 0.0) || !isfinite(sp)) {
+        fail = 1;
+      } else {
+        Lf[tri_idx(j, j)] = sqrt(sp);
+        rdiag[j] = 1.0 / Lf[tri_idx(j, j)];
       }
-      __syncthreads();
+    };
+    if (tid == 0) pivot(0, Lf[0]);
+    __syncthreads();
+    for (int j = 0; j < me; ++j) {
       if (fail) break;
       for (int i = j + 1 + tid; i < me; i += NT) {
         const double lij = Lf[tri_idx(i, j)] * rdiag[j];
@@ -487,7 +489,10 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       for (int a = j + 1 + cwp; a < me; a += NT / 32) {
         const double laj = colj[a];
         double* row = Lf + tri_idx(a, 0);
-        for (int b = j + 1 + cln; b <= a; b += 32) row[b] -= laj * colj[b];
+        for (int b = j + 1 + cln; b <= a; b += 32) {
+          row[b] -= laj * colj[b];
+          if (b == j + 1 && a == j + 1) pivot(j + 1, row[b]);
+        }
       }
       __syncthreads();
     }
@@ -559,7 +564,51 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
         if (lan + 32 * c < me) scaled(k, lan + 32 * c, yh[c], yl[c]);
     };
     constexpr int kWarps = NT / 32;
-    for (int k = 0; k < me - 1; ++k) {  // forward: rows below the pivot
+    // Two pivots per barrier: every thread also forms, for its own columns,
+    // the second pivot row's value after the first pivot's update (t, with
+    // the same operations as `update`) and its scaled value; rows past both
+    // pivots then take both updates in order, and the second pivot row's
+    // owner stores t after the barrier (no one reads that row again before
+    // the next pass, which follows a barrier).
+    float y2h[kCols], y2l[kCols], t2h[kCols], t2l[kCols];
+    auto second_pivot = [&](int k2, float2 l) {  // row k2 after the update by pivot y
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const int j = lan + 32 * c;
+        if (j < me) {
+          const float2 w = W[k2 * me + j];
+          float ph, pl;
+          df_mul(l.x, l.y, yh[c], yl[c], ph, pl);
+          df_add(w.x, w.y, -ph, -pl, t2h[c], t2l[c]);
+          df_mul(t2h[c], t2l[c], rd2[k2].x, rd2[k2].y, y2h[c], y2l[c]);
+        }
+      }
+    };
+    auto store_second = [&](int k2) {
+      if (k2 % kWarps == wrp) {
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (lan + 32 * c < me) W[k2 * me + lan + 32 * c] = make_float2(t2h[c], t2l[c]);
+      }
+    };
+    int k = 0;
+    for (; k + 1 < me - 1; k += 2) {  // forward: rows below the pivots
+      pivot_row(k);
+      second_pivot(k + 1, L2[tri_idx(k + 1, k)]);
+      const int i0 = wrp > k + 1 ? wrp : wrp + ((k + 1 - wrp) / kWarps + 1) * kWarps;
+      for (int i = i0; i < me; i += kWarps) {
+        const float2 l0 = L2[tri_idx(i, k)], l1 = L2[tri_idx(i, k + 1)];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (lan + 32 * c < me) {
+            update(i, lan + 32 * c, l0, yh[c], yl[c]);
+            update(i, lan + 32 * c, l1, y2h[c], y2l[c]);
+          }
+      }
+      __syncthreads();
+      store_second(k + 1);
+    }
+    for (; k < me - 1; ++k) {  // the last pivot, when the count is odd
       pivot_row(k);
       const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kWarps + 1) * kWarps;
       for (int i = i0; i < me; i += kWarps) {
@@ -570,6 +619,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
       __syncthreads();
     }
+    __syncthreads();
     for (int i = wrp; i < me; i += kWarps)  // Y = W / diag(L)
       for (int j = lan; j < me; j += 32) {
         float h, l;
@@ -577,7 +627,22 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
         W[i * me + j] = make_float2(h, l);
       }
     __syncthreads();
-    for (int k = me - 1; k > 0; --k) {  // backward: rows above the pivot
+    for (k = me - 1; k - 1 > 0; k -= 2) {  // backward: rows above the pivots
+      pivot_row(k);
+      second_pivot(k - 1, L2[tri_idx(k, k - 1)]);  // (L^T)_{k-1,k} = L_{k,k-1}
+      for (int i = wrp; i < k - 1; i += kWarps) {
+        const float2 l0 = L2[tri_idx(k, i)], l1 = L2[tri_idx(k - 1, i)];  // (L^T)_ik = L_ki
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+          if (lan + 32 * c < me) {
+            update(i, lan + 32 * c, l0, yh[c], yl[c]);
+            update(i, lan + 32 * c, l1, y2h[c], y2l[c]);
+          }
+      }
+      __syncthreads();
+      store_second(k - 1);
+    }
+    for (; k > 0; --k) {  // the last pivot, when the count is odd
       pivot_row(k);
       for (int i = wrp; i < k; i += kWarps) {
         const float2 lki = L2[tri_idx(k, i)];  // (L^T)_ik = L_ki
@@ -587,6 +652,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
       __syncthreads();
     }
+    __syncthreads();
     for (int pair = tid; pair < me * me; pair += NT) {  // M = W / diag(L)
       const int i = pair / me, j = pair - i * me;
       float h, l;
