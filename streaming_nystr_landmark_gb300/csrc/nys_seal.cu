@@ -12,14 +12,17 @@
 //     workspace for step 2 as (hi, lo) pairs, their f32 roundings to the
 //     state.
 //  2. pinv_kernel, one block per (group, head): A = exp(Q~64 K~64^T * scale)
-//     to f64 accuracy, then M = (A^T A + lambda I)^-1 A^T (fn ridge_pinv):
+//     to f64 accuracy (double-float arithmetic), then
+//     M = (A^T A + lambda I)^-1 A^T (fn ridge_pinv):
 //     lambda = 1e-6 * max(mean diag(A^T A), DBL_MIN); a failed Cholesky
 //     (pivot not > 0 or not finite, fn cholesky) multiplies lambda by ten, at
 //     most twelve attempts, then M = I / max(mean diag, DBL_MIN).  The
 //     Cholesky keeps the page's summation order.
 //  3. replay_kernel (or, for long prompts, replay_tc_kernel in
-//     nys_replay_tc.cu), one block per (group, head): the replay of positions
-//     sink..t-1 through the ring leaves keys sink..t-w-1 in the far field
+//     nys_replay_tc.cu), one block per group and value tile for up to 64
+//     landmark rows (several heads of a group; more heads take more blocks):
+//     the replay of positions sink..t-1 through the ring leaves keys
+//     sink..t-w-1 in the far field
 //     (NystromState::advance -> NystromHead::far_insert).  The state that
 //     sequential loop produces is m_max_i = max_j l_ij, Z^_i = sum_j
 //     exp(l_ij - m_max_i), T^_i = sum_j exp(l_ij - m_max_i) v_j with
@@ -563,7 +566,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       for (int c = 0; c < kCols; ++c)
         if (lan + 32 * c < me) scaled(k, lan + 32 * c, yh[c], yl[c]);
     };
-    constexpr int kWarps = NT / 32;
+    constexpr int kPinvWarps = NT / 32;
     // Two pivots per barrier: every thread also forms, for its own columns,
     // the second pivot row's value after the first pivot's update (t, with
     // the same operations as `update`) and its scaled value; rows past both
@@ -585,7 +588,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       }
     };
     auto store_second = [&](int k2) {
-      if (k2 % kWarps == wrp) {
+      if (k2 % kPinvWarps == wrp) {
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
           if (lan + 32 * c < me) W[k2 * me + lan + 32 * c] = make_float2(t2h[c], t2l[c]);
@@ -595,8 +598,8 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     for (; k + 1 < me - 1; k += 2) {  // forward: rows below the pivots
       pivot_row(k);
       second_pivot(k + 1, L2[tri_idx(k + 1, k)]);
-      const int i0 = wrp > k + 1 ? wrp : wrp + ((k + 1 - wrp) / kWarps + 1) * kWarps;
-      for (int i = i0; i < me; i += kWarps) {
+      const int i0 = wrp > k + 1 ? wrp : wrp + ((k + 1 - wrp) / kPinvWarps + 1) * kPinvWarps;
+      for (int i = i0; i < me; i += kPinvWarps) {
         const float2 l0 = L2[tri_idx(i, k)], l1 = L2[tri_idx(i, k + 1)];
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
@@ -610,8 +613,8 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
     for (; k < me - 1; ++k) {  // the last pivot, when the count is odd
       pivot_row(k);
-      const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kWarps + 1) * kWarps;
-      for (int i = i0; i < me; i += kWarps) {
+      const int i0 = wrp > k ? wrp : wrp + ((k - wrp) / kPinvWarps + 1) * kPinvWarps;
+      for (int i = i0; i < me; i += kPinvWarps) {
         const float2 lik = L2[tri_idx(i, k)];
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
@@ -620,7 +623,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
       __syncthreads();
     }
     __syncthreads();
-    for (int i = wrp; i < me; i += kWarps)  // Y = W / diag(L)
+    for (int i = wrp; i < me; i += kPinvWarps)  // Y = W / diag(L)
       for (int j = lan; j < me; j += 32) {
         float h, l;
         scaled(i, j, h, l);
@@ -630,7 +633,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     for (k = me - 1; k - 1 > 0; k -= 2) {  // backward: rows above the pivots
       pivot_row(k);
       second_pivot(k - 1, L2[tri_idx(k, k - 1)]);  // (L^T)_{k-1,k} = L_{k,k-1}
-      for (int i = wrp; i < k - 1; i += kWarps) {
+      for (int i = wrp; i < k - 1; i += kPinvWarps) {
         const float2 l0 = L2[tri_idx(k, i)], l1 = L2[tri_idx(k - 1, i)];  // (L^T)_ik = L_ki
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
@@ -644,7 +647,7 @@ pinv_kernel(DevState s, int64_t g0, SealGeom sg, const double* __restrict__ ws) 
     }
     for (; k > 0; --k) {  // the last pivot, when the count is odd
       pivot_row(k);
-      for (int i = wrp; i < k; i += kWarps) {
+      for (int i = wrp; i < k; i += kPinvWarps) {
         const float2 lki = L2[tri_idx(k, i)];  // (L^T)_ik = L_ki
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
