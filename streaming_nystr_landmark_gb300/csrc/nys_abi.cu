@@ -24,6 +24,7 @@ struct nys_states {
   int debug_skip;                  // test hook for the next decode launch
   int debug_replay;                // test hook for the next seal's replay
   int device;
+  nys::SealFork fork;              // the seal's second stream, made at the first seal
 };
 
 namespace {
@@ -32,6 +33,27 @@ constexpr size_t kAlign = 256;
 constexpr size_t kWorkspaceBudget = size_t(512) << 20;  // per seal chunk
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// The seal's side stream and its two events, made once per handle; if any
+// of them cannot be made the seal stays on the caller's stream.
+const nys::SealFork& seal_fork(nys_states* st) {
+  nys::SealFork& f = st->fork;
+  bool failed = false;
+  if (!f.side && cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess) {
+    f.side = nullptr;
+    failed = true;
+  }
+  if (!f.forked && cudaEventCreateWithFlags(&f.forked, cudaEventDisableTiming) != cudaSuccess) {
+    f.forked = nullptr;
+    failed = true;
+  }
+  if (!f.joined && cudaEventCreateWithFlags(&f.joined, cudaEventDisableTiming) != cudaSuccess) {
+    f.joined = nullptr;
+    failed = true;
+  }
+  if (failed) cudaGetLastError();  // only this call's failure: no second stream
+  return f;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -258,6 +280,9 @@ int nys_free_states(nys_states* st) {
   if (!st) return NYS_OK;
   int rc = NYS_OK;
   if (st->owned && st->base && cudaFree(st->base) != cudaSuccess) rc = NYS_E_CUDA;
+  if (st->fork.side && cudaStreamDestroy(st->fork.side) != cudaSuccess) rc = NYS_E_CUDA;
+  if (st->fork.forked && cudaEventDestroy(st->fork.forked) != cudaSuccess) rc = NYS_E_CUDA;
+  if (st->fork.joined && cudaEventDestroy(st->fork.joined) != cudaSuccess) rc = NYS_E_CUDA;
   delete st;
   return rc;
 }
@@ -313,7 +338,7 @@ int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
     const int64_t nb = std::min(chunk, n - a);
     e = nys::launch_seal(ds, g0 + a, nb, t, m_eff, q + a * H * (int64_t)t * c.d,
                          k + a * (int64_t)t * c.d, v + a * (int64_t)t * c.dv,
-                         static_cast<double*>(ws), s, a == 0 ? stall : 0);
+                         static_cast<double*>(ws), s, a == 0 ? stall : 0, seal_fork(st));
   }
   const cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess || ef != cudaSuccess) return NYS_E_CUDA;
@@ -383,7 +408,8 @@ int nys_seal_ragged(nys_states* st, int64_t g0, int64_t n, const int32_t* t_host
   for (int64_t a = 0; a < n && e == cudaSuccess; a += chunk) {
     const int64_t nb = std::min(chunk, n - a);
     const nys::SealGeom sg{0, 0, t_dev + a, me_dev + a, off_dev + a};
-    e = nys::launch_seal_geom(ds, g0 + a, nb, sg, max_me, q, k, v, static_cast<double*>(ws), s);
+    e = nys::launch_seal_geom(ds, g0 + a, nb, sg, max_me, q, k, v, static_cast<double*>(ws), s,
+                              0, seal_fork(st));
   }
   const cudaError_t f1 = cudaFreeAsync(ws, s), f2 = cudaFreeAsync(meta, s);
   // The host arrays above were staged by the copies before they returned.

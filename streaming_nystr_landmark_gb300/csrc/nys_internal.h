@@ -231,22 +231,37 @@ cudaError_t launch_exact_step(const DevState& s, int64_t g0, int64_t n, const fl
 // head's query landmarks before rounding).
 size_t seal_workspace_bytes_per_group(const DevState& s);
 
+// A second stream for the seal: the pinv (which needs the landmarks) and the
+// replay (which needs Q~ but not M) are independent, so the pinv runs on
+// `side` next to the replay on the caller's stream (measured: long seal
+// 86.8 -> 85.7 ms, a ragged m = 64 batch 5.29 -> 5.08 ms, the rest within
+// 1%; with the replay on a high-priority side stream instead, slower).  The
+// seal forks `side` from the caller's stream after the landmarks and joins
+// it back before it returns; null members keep everything on one stream.
+struct SealFork {
+  cudaStream_t side = nullptr;
+  cudaEvent_t forked = nullptr, joined = nullptr;
+  bool on() const { return side && forked && joined; }
+};
+
 // Seal groups [g0, g0+n) with prompt length t and m_eff landmarks, using
 // `ws` (seal_workspace_bytes_per_group * n bytes) as f64 scratch.  Three
-// kernel launches on `stream`.
+// kernel launches on `stream` (the pinv on fork.side when fork is on; the
+// call returns with `stream` ordered after all of them).
 // debug_stall (test hook): the tensor-core replay's first CTA withholds its
 // first MMA, so its bounded waits run out (status 3 for its group).
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
                         const float* v, double* ws, cudaStream_t stream,
-                        int debug_stall = 0);
+                        int debug_stall = 0, const SealFork& fork = SealFork());
 
 // Seal with per-group prompt geometry (sg's arrays on the device, indexed
 // from 0 for group g0); max_me bounds every group's m_eff.  q, k, v point at
 // the start of the packed batch.
 cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
                              int max_me, const float* q, const float* k, const float* v,
-                             double* ws, cudaStream_t stream, int debug_stall = 0);
+                             double* ws, cudaStream_t stream, int debug_stall = 0,
+                             const SealFork& fork = SealFork());
 
 // Tensor-core replay (nys_replay_tc.cu): whether the geometry fits it
 // (m >= 32, d and dv <= 128 in multiples of 32), and its launch.  It takes

@@ -1012,17 +1012,13 @@ size_t seal_workspace_bytes_per_group(const DevState& s) {
   return (size_t)(1 + s.heads) * s.m * s.d * sizeof(double);
 }
 
-cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
-                             int max_me, const float* q, const float* k, const float* v,
-                             double* ws, cudaStream_t stream, int debug_stall) {
-  if (n <= 0) return cudaSuccess;
-  cudaError_t e;
-  landmarks_kernel<<<dim3((unsigned)n, 1 + s.heads), kThreads, 0, stream>>>(s, g0, sg, q, k, v,
-                                                                            ws);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+namespace {
 
+cudaError_t launch_pinv(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg, int max_me,
+                        double* ws, cudaStream_t stream) {
   // Up to 32 landmarks: 128-thread CTAs, eight per SM, so that the serial
   // steps of one head's Cholesky overlap with more heads' parallel work.
+  cudaError_t e;
   const size_t pbytes = pinv_smem_doubles(max_me) * sizeof(double);
   if (max_me <= 32) {
     if ((e = ensure_smem<pinv_kernel<128, 32>>(pbytes)) != cudaSuccess) return e;
@@ -1032,12 +1028,17 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
     pinv_kernel<kThreads, kMaxM><<<(unsigned)(n * s.heads), kThreads, pbytes, stream>>>(
         s, g0, sg, ws);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
-  // Replay: tensor cores for groups with long prompts (where the geometry
-  // fits), CUDA cores for the rest.  A uniform batch launches only the path
-  // its prompt length takes; a ragged one launches both, and each skips the
-  // other's groups.
+// Replay: tensor cores for groups with long prompts (where the geometry
+// fits), CUDA cores for the rest.  A uniform batch launches only the path
+// its prompt length takes; a ragged one launches both, and each skips the
+// other's groups.
+cudaError_t launch_replays(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
+                           const float* k, const float* v, cudaStream_t stream,
+                           int debug_stall) {
+  cudaError_t e;
   const bool tc = replay_tc_fits(s);
   const bool uniform = sg.t_arr == nullptr;
   const bool long_prompt = sg.t - s.w - s.sink >= kReplayTcMinKeys;
@@ -1052,11 +1053,41 @@ cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const Sea
   return launch_replay<4>(s, g0, n, sg, k, v, skip_long, stream);
 }
 
+}  // namespace
+
+cudaError_t launch_seal_geom(const DevState& s, int64_t g0, int64_t n, const SealGeom& sg,
+                             int max_me, const float* q, const float* k, const float* v,
+                             double* ws, cudaStream_t stream, int debug_stall,
+                             const SealFork& fork) {
+  if (n <= 0) return cudaSuccess;
+  cudaError_t e;
+  landmarks_kernel<<<dim3((unsigned)n, 1 + s.heads), kThreads, 0, stream>>>(s, g0, sg, q, k, v,
+                                                                            ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!fork.on()) {
+    if ((e = launch_pinv(s, g0, n, sg, max_me, ws, stream)) != cudaSuccess) return e;
+    return launch_replays(s, g0, n, sg, k, v, stream, debug_stall);
+  }
+  // The pinv on the side stream, the replay on the caller's; both follow
+  // the landmarks, and the caller's stream waits for the pinv before the
+  // next chunk's landmarks overwrite the workspace it reads.
+  if ((e = cudaEventRecord(fork.forked, stream)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(fork.side, fork.forked, 0)) != cudaSuccess) return e;
+  const cudaError_t ep = launch_pinv(s, g0, n, sg, max_me, ws, fork.side);
+  const cudaError_t ej = cudaEventRecord(fork.joined, fork.side);
+  const cudaError_t er = launch_replays(s, g0, n, sg, k, v, stream, debug_stall);
+  const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(stream, fork.joined, 0) : ej;
+  if (ep != cudaSuccess) return ep;
+  if (er != cudaSuccess) return er;
+  return ew;
+}
+
 cudaError_t launch_seal(const DevState& s, int64_t g0, int64_t n, int t,
                         int m_eff, const float* q, const float* k,
-                        const float* v, double* ws, cudaStream_t stream, int debug_stall) {
+                        const float* v, double* ws, cudaStream_t stream, int debug_stall,
+                        const SealFork& fork) {
   const SealGeom sg{t, m_eff, nullptr, nullptr, nullptr};
-  return launch_seal_geom(s, g0, n, sg, m_eff, q, k, v, ws, stream, debug_stall);
+  return launch_seal_geom(s, g0, n, sg, m_eff, q, k, v, ws, stream, debug_stall, fork);
 }
 
 }  // namespace nys
