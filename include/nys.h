@@ -166,8 +166,9 @@ int nys_memory_bytes(const nys_config* cfg, int64_t n_groups,
 int nys_alloc_states(const nys_config* cfg, int64_t n_groups, void* dev_buf,
                      size_t buf_bytes, nys_states** out);
 
-/* Destroy a handle, and the buffer if the library allocated it.  The caller
- * must make sure no enqueued work still uses it.  NULL is a no-op. */
+/* Destroy a handle, and the buffer if the library allocated it, and the
+ * second stream and two events its seals use.  The caller must make sure no
+ * enqueued work still uses it.  NULL is a no-op. */
 int nys_free_states(nys_states* st);
 
 /* Seal groups [g0, g0+n) on a prompt of t positions (nystrom.rs,
@@ -193,8 +194,11 @@ int nys_free_states(nys_states* st);
  * that would exceed exact_cap keys.
  * All n groups share t.  Re-sealing a group replaces its state.  Allocates a
  * temporary f64 workspace of n*m*d*8 bytes with cudaMallocAsync on `stream`
- * and frees it there.  Writes no attention output (the page's prefill
- * writes none).
+ * and frees it there.  The pinv kernel runs on a second stream owned by the
+ * handle (made at its first seal), forked from `stream` and joined back
+ * before the call returns, so all of the seal's work is ordered on `stream`
+ * as usual; calls on one handle must not overlap.  Writes no attention
+ * output (the page's prefill writes none).
  * Errors: NYS_E_INVAL, NYS_E_RANGE, NYS_E_EXACT_ONLY, NYS_E_ALIGN,
  * NYS_E_CUDA. */
 int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t,
