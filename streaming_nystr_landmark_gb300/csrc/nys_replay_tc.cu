@@ -387,12 +387,16 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
         bm = fmaxf(bm, sv[jx]);
       }
       const float nm = fmaxf(mrow, bm);
-      const float alpha = (mrow == -INFINITY) ? 0.f : expf(mrow - nm);
+      // Every exponent is <= 0 and the running sum always holds a term of 1
+      // (the key that set the maximum), so the fast exponential (__expf:
+      // about 2 ulp near 0, its error growing with |x| only where e^x is far
+      // below the sum's rounding) keeps the sums to fp32 accuracy.
+      const float alpha = (mrow == -INFINITY) ? 0.f : __expf(mrow - nm);
       mrow = nm;
       float zb = 0.f;
 #pragma unroll
       for (int jx = 0; jx < kTcKeys; ++jx) {
-        sv[jx] = (jx < nb) ? expf(sv[jx] - nm) : 0.f;
+        sv[jx] = (jx < nb) ? __expf(sv[jx] - nm) : 0.f;
         zb += sv[jx];
       }
       float nh, nl;
