@@ -495,13 +495,16 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       // Rows before kend are keys (dotted with every head's query); the rest
       // are Q~ rows, each dotted with the evicted key only.
       const int kend = min(nrow, max(0, ns + w + m - r0));
-      for (int base = 0; base < kend; base += kCWarps * kRowsPerRound) {
-        float x[kRowsPerRound * HT];
+      // Eight heads: two rows per round (16 partial sums) keep the loop within
+      // the 96 registers of two CTAs per SM; four rows spilled.
+      constexpr int kRR = HT > 4 ? 2 : kRowsPerRound;
+      for (int base = 0; base < kend; base += kCWarps * kRR) {
+        float x[kRR * HT];
 #pragma unroll
-        for (int i = 0; i < kRowsPerRound * HT; ++i) x[i] = 0.f;
+        for (int i = 0; i < kRR * HT; ++i) x[i] = 0.f;
 #pragma unroll
-        for (int u = 0; u < kRowsPerRound; ++u) {
-          const int lr = base + warp * kRowsPerRound + u;
+        for (int u = 0; u < kRR; ++u) {
+          const int lr = base + warp * kRR + u;
           if (lr < kend && ck) {
             const int vr = r0 + lr;
             const float* row = (vr - ns == slot && vr >= ns) ? xknew : stage + (size_t)lr * d;
@@ -510,11 +513,11 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             for (int hh = 0; hh < HT; ++hh) x[u * HT + hh] = dot4(a, qr[hh]);
           }
         }
-        const float tot = reduce_multi<kRowsPerRound * HT>(x, lane);
-        if (reduce_writer<kRowsPerRound * HT>(lane)) {
-          const int vi = reduce_index<kRowsPerRound * HT>(lane);
+        const float tot = reduce_multi<kRR * HT>(x, lane);
+        if (reduce_writer<kRR * HT>(lane)) {
+          const int vi = reduce_index<kRR * HT>(lane);
           const int u = vi / HT, hh = vi - u * HT;
-          const int lr = base + warp * kRowsPerRound + u;
+          const int lr = base + warp * kRR + u;
           if (lr < kend && hh < H) {
             const int vr = r0 + lr;
             const float l = tot * scale;
