@@ -27,9 +27,9 @@
 //      running max, rescale alpha, p = exp(s - m), Z^ fold, p split into
 //      three planes [row][key] in the K block's shared memory;
 //   4. one thread: O = P V as 6 * 4 MMAs (M=128, N=dv) into TMEM;
-//   5. both warpgroups (half the columns each): (hi, lo) <- (hi, lo) * alpha
-//      + O (Kahan-compensated), with hi and lo kept in TMEM; warpgroup 1
-//      then splits the next K block into the key planes.
+//   5. warpgroup 0 (thread = row): (hi, lo) <- (hi, lo) * alpha + O
+//      (Kahan-compensated) on every column, with hi and lo kept in TMEM,
+//      while warpgroup 1 splits the next K block into the key planes.
 // Every wait on an MMA is bounded (2 s of %globaltimer); a timeout sets the
 // group's status word and the CTA stops, frees its tensor memory and
 // returns.
@@ -431,10 +431,13 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
     ok = __all_sync(0xffffffffu, tc_wait(&bar_o, parity, vabort));
     if (!ok) abort_flag = 1;
     tc_fence_after();
-    // 5. (hi, lo) <- (hi, lo) * alpha + O on this thread's column half.
-    if (ok) {
+    // 5. warpgroup 0: (hi, lo) <- (hi, lo) * alpha + O on every column of
+    //    its row, while
+    // 1'. warpgroup 1 splits the prefetched key block into the key planes
+    //     (the P V that read them as p is complete).
+    if (ok && half == 0) {
       const float alpha = alpha_s[row];
-      for (int c = half * cols_half; c < (half + 1) * cols_half; c += 16) {
+      for (int c = 0; c < dv; c += 16) {
         float o[16], hi[16], lo[16];
         tc_ld16(lane_base + kColO + c, o);
         tc_ld16(lane_base + kColHi + c, hi);
@@ -446,8 +449,6 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
       }
       tc_wait_st();
     }
-    // 1'. warpgroup 1: the prefetched key block into the key planes (the
-    //     P V that read them as p is complete).
     if (half == 1 && ok && more) k_store(tid - kTcThreads / 2, kTcThreads / 2, kpre, kKPre);
     tc_fence_before();
     __syncthreads();
