@@ -659,7 +659,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       const float* stage = reinterpret_cast<const float*>(stage_ptr(ci));
       const int r0 = st * P.rows_v;
       const int nrow = min(P.rows_v, ns + w - r0);
-#pragma unroll (HT <= 2 ? 4 : 1)
+#pragma unroll (HT <= 2 ? 4 : 2)
       for (int lr = warp; lr < nrow; lr += kCWarps) {
         const int j = r0 + lr;  // near row: sinks first, then window slots
         if (j < nnear && cv) {
