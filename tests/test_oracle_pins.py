@@ -412,8 +412,85 @@ def test_nystrom_reproduction_special_case():
         err = np.abs(out[0] - ref).max() / np.abs(ref).max()
         worst = max(worst, err)
     assert worst < 2e-5, worst
-    # ... and the bound is not vacuous: a wrong M (transposed, or plain
-    # inverse-free identity) misses it by orders of magnitude.
+    assert o.far_len(0) == t - sink - w + 40
+    # Au is symmetric here, so so is M: this case cannot tell M from its
+    # transpose.  test_nystrom_reproduction_nonsymmetric below does.
+
+
+def _nonsym_landmarks(m, alpha, beta, seed):
+    """Key landmarks alpha*(I + 0.5 U) with U strictly upper triangular
+    (entries in [0.5, 1]) and query landmarks beta*I: Au[i][j] =
+    exp(q~_i . k~_j * scale) then has exp(0) = 1 below the diagonal and up to
+    exp(alpha*beta*scale/2) above it -- far from symmetric, yet dominated by
+    its diagonal and well conditioned."""
+    rng = np.random.default_rng(seed)
+    upper = np.triu(rng.uniform(0.5, 1.0, (m, m)), 1)
+    k_t = (alpha * (np.eye(m) + 0.5 * upper)).astype(np.float32)
+    q_t = (beta * np.eye(m)).astype(np.float32)
+    return k_t, q_t
+
+
+def test_nystrom_reproduction_nonsymmetric():
+    """Nystrom reproduction with a NON-symmetric landmark kernel, which pins
+    the orientation of M.  The prompt is segment-constant: segment b holds
+    keys k~_b and queries q~_b, so seg_means returns exactly those rows.  The
+    page builds Au with query landmarks as rows (nystrom.rs,
+    ``NystromHead::seal``), solves G M = Au^T so that M's rows are key
+    landmarks (``ridge_pinv``), and mixes u_b = sum_a F_a M[a][b]
+    (``NystromHead::step``).  A far key equal to k~_b then gets the weight
+    F (M Au) e_b, and M Au = (Au^T Au + lam I)^-1 Au^T Au is I up to the
+    ridge error eps = lam / (sigma_min^2 + lam): every far weight equals the
+    exact weight exp(q . k_j * scale) and the output equals softmax attention
+    over all keys.  Building Au transposed, or mixing u = M F, replaces M Au
+    by M^T Au, which is off the identity by several percent here.  Aggregate
+    only: Fm clamps the negative entries of u = F Au^-1 and so leaves the
+    reproduction identity by design."""
+    rect = AGGREGATE
+    m = d = dv = 8
+    t, w, sink = 64, 16, 4
+    alpha = beta = 4.0
+    k_t, q_t = _nonsym_landmarks(m, alpha, beta, seed=5)
+    seg = np.repeat(np.arange(m), t // m)
+    k = k_t[seg]
+    qh = q_t[seg][None]
+    rng = np.random.default_rng(22)
+    v = rng.standard_normal((t, dv)).astype(np.float32)
+    o = NystromOracle(m=m, w=w, sink=sink, heads=1, rect=rect)
+    o.prefill(qh, k, v)
+    np.testing.assert_array_equal(o.k_tilde, k_t.astype(np.float64))
+    np.testing.assert_array_equal(o.hs[0].q_tilde, q_t.astype(np.float64))
+    scale = o.scale
+    au = np.exp((q_t.astype(np.float64) @ k_t.astype(np.float64).T) * scale)
+    assert np.abs(au - au.T).max() > 0.04 * np.abs(au).max()
+    sv = np.linalg.svd(au, compute_uv=False)
+    lam = 1e-6 * float(np.sum(au * au)) / m
+    eps = lam / (sv[-1] ** 2 + lam)
+    assert eps < 1e-5
+    keys, vals = list(k.astype(np.float64)), list(v.astype(np.float64))
+    worst = worst_w = 0.0
+    for n in range(40):
+        qa = rng.standard_normal((1, d)).astype(np.float32)
+        kn = k_t[rng.integers(m)]
+        vn = rng.standard_normal(dv).astype(np.float32)
+        out = o.step(qa, kn, vn)
+        keys.append(kn.astype(np.float64))
+        vals.append(vn.astype(np.float64))
+        q64 = qa[0].astype(np.float64)
+        ref = softmax_attention(q64, np.array(keys), np.array(vals), scale)
+        worst = max(worst, np.abs(out[0] - ref).max() / np.abs(ref).max())
+        # The materialised far weights themselves are the exact ones.
+        kh = np.array(keys)
+        _, far_w, keep = direct_output(q64, kh, np.array(vals), sink, w,
+                                       o.k_tilde, o.hs[0].q_tilde,
+                                       o.hs[0].mu, scale, rect)
+        p = kh.shape[0] - 1
+        exact_w = np.exp((kh[sink:p - w + 1] @ q64) * scale)
+        assert keep
+        worst_w = max(worst_w,
+                      np.abs(far_w - exact_w).max() / exact_w.max())
+    # eps bounds |F (M Au - I) e_b| / |F|; M's f32 storage adds ~1e-7.
+    assert worst_w < 10 * eps + 1e-6, (worst_w, eps)
+    assert worst < 2e-5, worst
     assert o.far_len(0) == t - sink - w + 40
 
 
