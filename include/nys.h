@@ -239,14 +239,20 @@ int nys_step_batch(nys_states* st, int64_t g0, int64_t n, const float* q,
  * while they run -- a serving loop that has reserved all memory up front, an
  * allocator that forbids cudaMalloc/cudaMallocAsync inside its critical
  * section, or code embedded in a host application that owns every buffer.
- * It computes exactly what nys_seal computes (same kernels, same checks,
- * same results), but its f64 landmark workspace is a 4 MiB array that the
+ * It computes exactly what nys_seal computes (same kernels, the same checks
+ * from one shared function, bit-identical states), but its f64 landmark
+ * workspace is a 4 MiB array that the
  * library places in device global memory at load time (every GPU that loads
  * the library keeps those 4 MiB until the process exits).  Groups are sealed
  * in chunks that fit the array, one after another on `stream`.
  *  - The first call on a device looks the array's device address up
  *    (cudaGetSymbolAddress) with that device current and caches it; make
- *    that first call before any stream capture on the device.
+ *    that first call before any stream capture on the device.  The cached
+ *    address belongs to the device's context as it was then: after a
+ *    cudaDeviceReset (or any teardown of that context) it is stale, so do
+ *    not call nys_seal_static again in a process that reset the device.
+ *  - Exact-only prompts (t <= w + sink + 8 on a handle with exact_cap > 0)
+ *    need no workspace; they are sealed exactly as nys_seal seals them.
  *  - Every call on a device shares the one array, and each call overwrites
  *    what the previous one left there.  Calls that may run at the same time
  *    on the GPU (different streams without ordering between them) race on

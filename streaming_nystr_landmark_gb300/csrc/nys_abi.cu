@@ -164,26 +164,51 @@ void forget_exact(nys_states* st, int64_t g0, int64_t n) {
 
 namespace nys {
 
-int prepare_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
-                 const float* k, const float* v, DevState* ds, int* m_eff) {
-  if (!st || !ds || !m_eff) return NYS_E_INVAL;
+int plan_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
+              const float* k, const float* v, SealPlan* plan) {
+  if (!st || !plan) return NYS_E_INVAL;
   int rc = check_range(st, g0, n);
   if (rc) return rc;
   const nys_config& c = st->cfg;
   if (t < 1) return NYS_E_RANGE;
-  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) return NYS_E_EXACT_ONLY;
+  plan->ds = dev_state(st);
+  // nystrom.rs, prefill_shared: short prompts skip the skeleton entirely and
+  // keep every key exact (exact-only mode), which needs the exact region.
+  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) {
+    if (c.exact_cap == 0) return NYS_E_EXACT_ONLY;
+    if (t > c.exact_cap) return NYS_E_RANGE;
+    if (n > 0) {
+      if (!k || !v) return NYS_E_INVAL;
+      if (!aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
+    }
+    plan->exact = true;
+    plan->m_eff = 0;
+    return NYS_OK;
+  }
   if (n > 0) {
     if (!q || !k || !v) return NYS_E_INVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
   }
-  *m_eff = std::min(std::max(t / 8, 4), c.m);
-  if (n > 0 && *m_eff < c.m && !g_clamp_said.exchange(true)) {
+  plan->exact = false;
+  plan->m_eff = std::min(std::max(t / 8, 4), c.m);
+  if (n > 0 && plan->m_eff < c.m && !g_clamp_said.exchange(true)) {
     std::fprintf(stderr,
                  "nys: landmark budget m=%d clamped to m_eff=%d: the prompt is %d tokens and "
                  "the landmarks take t/8; seal at least %d tokens to use the whole budget\n",
-                 c.m, *m_eff, t, c.m * 8);
+                 c.m, plan->m_eff, t, c.m * 8);
   }
-  *ds = dev_state(st);
+  return NYS_OK;
+}
+
+int run_exact_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* k,
+                   const float* v, cudaStream_t stream) {
+  if (n == 0) return NYS_OK;
+  if (launch_exact_seal(dev_state(st), g0, n, t, k, v, stream) != cudaSuccess) return NYS_E_CUDA;
+  std::memset(st->sealed.data() + g0, 1, (size_t)n);
+  for (int64_t g = g0; g < g0 + n; ++g) {
+    if (st->exact_len[(size_t)g] < 0) ++st->n_exact;
+    st->exact_len[(size_t)g] = t;
+  }
   return NYS_OK;
 }
 
@@ -289,41 +314,15 @@ int nys_free_states(nys_states* st) {
 
 int nys_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
              const float* k, const float* v, void* stream) {
-  if (!st) return NYS_E_INVAL;
-  int rc = check_range(st, g0, n);
+  nys::SealPlan plan;
+  int rc = nys::plan_seal(st, g0, n, t, q, k, v, &plan);
   if (rc) return rc;
-  const nys_config& c = st->cfg;
-  if (t < 1) return NYS_E_RANGE;
-  // nystrom.rs, prefill_shared: short prompts skip the skeleton entirely and
-  // keep every key exact (exact-only mode), which needs the exact region.
-  if ((int64_t)t <= (int64_t)c.w + c.sink + 8) {
-    if (c.exact_cap == 0) return NYS_E_EXACT_ONLY;
-    if (t > c.exact_cap) return NYS_E_RANGE;
-    if (n == 0) return NYS_OK;
-    if (!k || !v) return NYS_E_INVAL;
-    if (!aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
-    if (nys::launch_exact_seal(dev_state(st), g0, n, t, k, v,
-                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return NYS_E_CUDA;
-    std::memset(st->sealed.data() + g0, 1, (size_t)n);
-    for (int64_t g = g0; g < g0 + n; ++g) {
-      if (st->exact_len[(size_t)g] < 0) ++st->n_exact;
-      st->exact_len[(size_t)g] = t;
-    }
-    return NYS_OK;
-  }
-  if (n == 0) return NYS_OK;
-  if (!q || !k || !v) return NYS_E_INVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return NYS_E_ALIGN;
-  const int m_eff = std::min(std::max(t / 8, 4), c.m);
-  if (m_eff < c.m && !g_clamp_said.exchange(true)) {
-    std::fprintf(stderr,
-                 "nys: landmark budget m=%d clamped to m_eff=%d: the prompt is %d tokens and "
-                 "the landmarks take t/8; seal at least %d tokens to use the whole budget\n",
-                 c.m, m_eff, t, c.m * 8);
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const nys::DevState ds = dev_state(st);
+  if (plan.exact) return nys::run_exact_seal(st, g0, n, t, k, v, s);
+  if (n == 0) return NYS_OK;
+  const nys_config& c = st->cfg;
+  const int m_eff = plan.m_eff;
+  const nys::DevState& ds = plan.ds;
   const size_t per = nys::seal_workspace_bytes_per_group(ds);
   int64_t chunk = (int64_t)(kWorkspaceBudget / per);
   if (chunk < 1) chunk = 1;

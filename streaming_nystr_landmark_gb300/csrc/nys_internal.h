@@ -274,13 +274,29 @@ cudaError_t launch_replay_tc(const DevState& s, int64_t g0, int64_t n, const Sea
                              const float* k, const float* v, cudaStream_t stream,
                              int debug_stall = 0);
 
-// Host-side checks of a seal request, identical to nys_seal's, for entry
-// points that supply their own workspace.  Fills the device view and m_eff
-// (printing the one-time clamp notice); returns a nys_status.
-int prepare_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
-                 const float* k, const float* v, DevState* ds, int* m_eff);
+// One uniform-length seal request after the host-side checks that every
+// seal entry point shares (nys_seal, nys_seal_static): range, prompt length,
+// pointers, alignment, and the page's mode choice (nystrom.rs,
+// prefill_shared).  `exact` marks an exact-only prompt (t <= w + sink + 8) on
+// a handle that has an exact region; otherwise the landmark path runs with
+// m_eff landmarks on the device view `ds`.
+struct SealPlan {
+  bool exact = false;
+  int m_eff = 0;
+  DevState ds;
+};
 
-// Host record that groups [g0, g0+n) hold a sealed state.
+// Check a seal request and fill `plan` (printing the one-time clamp notice
+// when m_eff < m and n > 0).  Returns a nys_status; nothing is enqueued.
+int plan_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* q,
+              const float* k, const float* v, SealPlan* plan);
+
+// Seal groups [g0, g0+n) in exact-only mode (no workspace needed) and record
+// them as exact-only groups on the host.  Returns a nys_status.
+int run_exact_seal(nys_states* st, int64_t g0, int64_t n, int32_t t, const float* k,
+                   const float* v, cudaStream_t stream);
+
+// Host record that groups [g0, g0+n) hold a landmark-path sealed state.
 void record_sealed(nys_states* st, int64_t g0, int64_t n);
 
 }  // namespace nys

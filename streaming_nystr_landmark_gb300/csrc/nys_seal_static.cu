@@ -27,7 +27,13 @@ double* scratch_address() {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_seal_scratch) != cudaSuccess || !p) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_seal_scratch) != cudaSuccess || !p) {
+      // Clear the runtime's sticky last error so that the next call of the
+      // library (which checks cudaGetLastError after its launches) does not
+      // report this failure as its own.
+      cudaGetLastError();
+      return nullptr;
+    }
     g_scratch_ptr[dev] = static_cast<double*>(p);
   }
   return g_scratch_ptr[dev];
@@ -38,10 +44,14 @@ double* scratch_address() {
 extern "C" int nys_seal_static(nys_states* st, int64_t g0, int64_t n, int32_t t,
                                const float* q, const float* k, const float* v,
                                void* stream) {
-  nys::DevState ds;
-  int m_eff = 0;
-  int rc = nys::prepare_seal(st, g0, n, t, q, k, v, &ds, &m_eff);
+  // The same checks and mode choice as nys_seal, from the same function.
+  nys::SealPlan plan;
+  int rc = nys::plan_seal(st, g0, n, t, q, k, v, &plan);
   if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Exact-only prompts copy the prompt into the state: no workspace at all.
+  if (plan.exact) return nys::run_exact_seal(st, g0, n, t, k, v, s);
+  const nys::DevState& ds = plan.ds;
   const size_t per = nys::seal_workspace_bytes_per_group(ds);
   if (per > kScratchBytes) return NYS_E_SCRATCH;
   if (n == 0) return NYS_OK;
@@ -52,11 +62,10 @@ extern "C" int nys_seal_static(nys_states* st, int64_t g0, int64_t n, int32_t t,
   // workspace element a kernel reads was written earlier in the same chunk,
   // so nothing left by a previous call is ever read.
   const int64_t chunk = std::min<int64_t>(n, (int64_t)(kScratchBytes / per));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t H = ds.heads;
   for (int64_t a = 0; a < n; a += chunk) {
     const int64_t nb = std::min(chunk, n - a);
-    if (nys::launch_seal(ds, g0 + a, nb, t, m_eff, q + a * H * (int64_t)t * ds.d,
+    if (nys::launch_seal(ds, g0 + a, nb, t, plan.m_eff, q + a * H * (int64_t)t * ds.d,
                          k + a * (int64_t)t * ds.d, v + a * (int64_t)t * ds.dv, ws, s) !=
         cudaSuccess)
       return NYS_E_CUDA;

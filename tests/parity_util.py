@@ -149,6 +149,30 @@ class ParityRun:
         self.st.close()
 
 
+def step_oracles_and_compare(oracles, tq, tk, tv, outs):
+    """Step each group's oracle once (host token inputs tq [G][H][d],
+    tk [G][d], tv [G][dv], group g feeding oracles[g]) and compare every
+    array in `outs` ([G][H][dv] device results copied to the host) with the
+    oracle's outputs row by row at OUT_TOL.  Rows on a discontinuity of the
+    method (guard band, near-weight underflow) are only checked finite.
+    Returns the worst row error."""
+    worst = 0.0
+    for g, o in enumerate(oracles):
+        ref = o.step(tq[g], tk[g], tv[g])
+        for h in range(ref.shape[0]):
+            dg = o.diags[-1][h]
+            flagged = abs(dg.margin) < GUARD_BAND or dg.near_gap > UNDERFLOW_GAP
+            for got in outs:
+                row = np.asarray(got[g][h], dtype=np.float64)
+                if flagged:
+                    assert np.all(np.isfinite(row)), (g, h)
+                    continue
+                err = row_err(row, ref[h])
+                assert err <= OUT_TOL, (g, h, err)
+                worst = max(worst, err)
+    return worst
+
+
 def read_state(st):
     """Host copies of every state region (T^ and Z^ as hi + lo)."""
     reg = {name: st.region(name).cpu().numpy() for name in (

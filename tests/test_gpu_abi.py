@@ -5,7 +5,8 @@ import numpy as np
 import pytest
 
 from oracle import NystromOracle
-from parity_util import OUT_TOL, compare_group_state, read_state, row_err
+from parity_util import (OUT_TOL, compare_group_state, read_state, row_err,
+                         step_oracles_and_compare)
 from streaming_nystr_landmark_gb300 import nys
 from streaming_nystr_landmark_gb300.workloads import (Workload, host_prompt_batch,
                                                       host_token_batch)
@@ -233,11 +234,17 @@ def test_host_pipeline_matches_direct_steps(cuda_device):
 def test_per_layer_launches_and_graph_replay_match_fused(cuda_device):
     """A model steps one layer at a time: per-layer handles stepped with one
     launch each, eagerly or replayed from a CUDA graph, give bit-identical
-    outputs and state to one fused launch over all layers' groups."""
+    outputs and state to one fused launch over all layers' groups, and every
+    output row of every token matches the fp64 oracle of its group."""
     import torch
     L, per = 3, 6
     wl = Workload("layers", 2, 32, 32, 8, 16, 4, 0, 64, 8, 1, 1, L * per, "unit2", seed=9)
     q, k, v, gens = host_prompt_batch(wl, range(L * per))
+    oracles = []
+    for g in range(L * per):
+        o = NystromOracle(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.rect)
+        o.prefill(q[g], k[g], v[g])
+        oracles.append(o)
     mk = lambda n: nys.NystromStates(wl.m, wl.w, wl.sink, 2, 32, 32, n, 0, cuda_device)
     fused = mk(L * per)
     fused.seal(*_to(cuda_device, q, k, v))
@@ -268,6 +275,7 @@ def test_per_layer_launches_and_graph_replay_match_fused(cuda_device):
     layered(graphed, out_g)
     torch.cuda.synchronize()
     assert torch.equal(out_f, out_e) and torch.equal(out_f, out_g)
+    step_oracles_and_compare(oracles, *th, [out_e.cpu().numpy(), out_g.cpu().numpy()])
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         layered(graphed, out_g)
@@ -281,6 +289,7 @@ def test_per_layer_launches_and_graph_replay_match_fused(cuda_device):
         torch.cuda.synchronize()
         assert torch.equal(out_f, out_e), n
         assert torch.equal(out_f, out_g), n
+        step_oracles_and_compare(oracles, *th, [out_e.cpu().numpy(), out_g.cpu().numpy()])
     for name in ("t_hat", "t_lo", "z_hat", "m_max", "far_len", "ints", "win_k"):
         whole = fused.region(name)
         for l in range(L):

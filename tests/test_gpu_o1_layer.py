@@ -2,10 +2,14 @@
 position at a time, seal when the page's preconditions hold, then decode.
 
 A layer sealed through the lifecycle must hold exactly the states a direct
-nys_seal of the same groups builds, and decode identically; every failed
+nys_seal of the same groups builds, decode identically, and match the fp64
+oracle run per (sequence, KV head) on the layer's own tensors; every failed
 precondition must leave the layer unsealed (exact), as o1_seal returns false."""
 import numpy as np
 import pytest
+
+from oracle import NystromOracle
+from parity_util import step_oracles_and_compare
 
 from streaming_nystr_landmark_gb300 import nys
 from streaming_nystr_landmark_gb300.workloads import Workload, host_prompt_batch, host_token_batch
@@ -60,6 +64,19 @@ def test_lifecycle_matches_direct_seal_and_decode(cuda_device):
     ours = torch.as_tensor(_Raw(base, lay.total_bytes), device=cuda_device)
     theirs = direct.buf[direct._off:direct._off + lay.total_bytes]
     assert torch.equal(ours, theirs)
+    # The oracle side reads the layer's own tensors and applies the page's
+    # rule itself (Struct LayerKvCache, o1_step: query head h belongs to KV
+    # group h / hpk): one oracle per (sequence b, KV head j), fed query heads
+    # j*hpk .. j*hpk + hpk - 1 of sequence b.
+    k_layer = k.reshape(B, NKV, T, D)
+    v_layer = v.reshape(B, NKV, T, D)
+    oracles = []
+    for b in range(B):
+        for j in range(NKV):
+            o = NystromOracle(M, W, SINK, HPK, 0)
+            o.prefill(np.stack([q_layer[b, h] for h in range(NH) if h // HPK == j]),
+                      k_layer[b, j], v_layer[b, j])
+            oracles.append(o)
     for n in range(8):
         tq, tk, tv = host_token_batch(gens, n)                   # per group
         q_all = dev(tq.reshape(B, NKV, HPK, D).reshape(B, NH, D))
@@ -69,6 +86,15 @@ def test_lifecycle_matches_direct_seal_and_decode(cuda_device):
         out_d = torch.empty((B * NKV, HPK, D), device=cuda_device)
         direct.step(dev(tq), dev(tk), dev(tv), out_d)
         assert torch.equal(out_l.reshape(-1), out_d.reshape(-1)), n
+        # Oracle inputs and outputs rebuilt from the layer view by the rule.
+        ql, kl, vl = q_all.cpu().numpy(), kn.cpu().numpy(), vn.cpu().numpy()
+        got = out_l.cpu().numpy()
+        oq = np.stack([np.stack([ql[b, h] for h in range(NH) if h // HPK == j])
+                       for b in range(B) for j in range(NKV)])
+        og = np.stack([np.stack([got[b, h] for h in range(NH) if h // HPK == j])
+                       for b in range(B) for j in range(NKV)])
+        step_oracles_and_compare(oracles, oq, kl.reshape(B * NKV, D),
+                                 vl.reshape(B * NKV, D), [og])
     layer.close()
     direct.close()
 
