@@ -53,10 +53,9 @@ def algorithmic_bytes(wl) -> int:
 def state_overhead_bytes(wl) -> int:
     """Bytes per group-step beyond the method's fp32 state that this
     implementation moves: the compensation (low) parts of the far
-    accumulators, T^ lo (one fp8 byte per element) and Z^ lo (fp32), each
-    read and written."""
+    accumulators, T^ lo (bf16) and Z^ lo (fp32), each read and written."""
     H, m, dv = wl.heads_per_kv, wl.m, wl.dv
-    return H * (2 * 1 * m * dv + 2 * 4 * m)
+    return H * (2 * 2 * m * dv + 2 * 4 * m)
 
 
 def workload_config(wl, extra=None):

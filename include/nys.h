@@ -101,10 +101,7 @@ typedef struct nys_states nys_states; /* opaque host handle */
  *   t_hat   f32 [G][H][m][dv]    far numerator at scale e^{-m_max} (high part)
  *   z_hat   f32 [G][H][m]        far denominator, same scale (high part)
  *   m_max   f32 [G][H][m]        per-landmark running max of far logits
- *   t_lo    u8  [G][H][m][dv]    low part of the far numerator: fp8 e4m3
- *                                (OCP E4M3, max 448) of lo * 2^(25 - E), E the
- *                                exponent of the row's z_hat high part,
- *                                clamped to [-27, 127]
+ *   t_lo    bf16 [G][H][m][dv]   low part of the far numerator
  *   z_lo    f32 [G][H][m]        low part of the far denominator
  *   exact_k f32 [G][exact_cap][d]   keys of exact-only groups (absent if 0)
  *   exact_v f32 [G][exact_cap][dv]  their values
@@ -122,13 +119,7 @@ typedef struct nys_states nys_states; /* opaque host handle */
  * drift roughly fifty-fold in the output, so over a thousand tokens plain f32
  * leaves the exact result by ~1e-4.  The low parts hold the rounding error of
  * each update (exact product and sum errors via FMA), which keeps the far
- * field within ~1e-7 of exact.  A low part is at most half an ulp of its high
- * part, so T^'s is stored in one byte: three significant bits at a per-row
- * power-of-two scale set by Z^ (T^_b is a weighted sum of values whose
- * weights sum to Z^_b, which bounds the row's magnitude); values above 112 in
- * magnitude saturate that byte and keep only part of their compensation.
- * The low parts add 6.4% to the decode's state bytes at the pages' default
- * geometry.
+ * field within ~1e-7 of exact at 12.5% more state bytes.
  */
 typedef struct {
   size_t total_bytes;

@@ -96,7 +96,7 @@ bool make_layout(const nys_config& c, int64_t G, nys_layout* L) {
   L->off_t_hat = region(g * H * m * c.dv * 4);
   L->off_z_hat = region(g * H * m * 4);
   L->off_m_max = region(g * H * m * 4);
-  L->off_t_lo = region(g * H * m * c.dv);
+  L->off_t_lo = region(g * H * m * c.dv * 2);
   L->off_z_lo = region(g * H * m * 4);
   L->off_far_len = region(g * H * 4);
   L->off_ints = region(g * nys::kIntsPerGroup * 4);
@@ -122,7 +122,7 @@ nys::DevState dev_state(const nys_states* st) {
   s.t_hat = reinterpret_cast<float*>(b + L.off_t_hat);
   s.z_hat = reinterpret_cast<float*>(b + L.off_z_hat);
   s.m_max = reinterpret_cast<float*>(b + L.off_m_max);
-  s.t_lo = reinterpret_cast<uint8_t*>(b + L.off_t_lo);
+  s.t_lo = reinterpret_cast<uint16_t*>(b + L.off_t_lo);
   s.z_lo = reinterpret_cast<float*>(b + L.off_z_lo);
   s.far_len = reinterpret_cast<int32_t*>(b + L.off_far_len);
   s.ints = reinterpret_cast<int32_t*>(b + L.off_ints);

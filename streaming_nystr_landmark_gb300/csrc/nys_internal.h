@@ -59,7 +59,7 @@ struct DevState {
   float* t_hat;
   float* z_hat;
   float* m_max;
-  uint8_t* t_lo;   // low part of t_hat: fp8 e4m3 of lo * tlo_scale(z_hat)
+  uint16_t* t_lo;  // bf16 bits: low part of t_hat
   float* z_lo;     // low part of z_hat
   int32_t* far_len;
   int32_t* ints;
@@ -175,58 +175,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// Storage of T^'s low part in one byte per element.  The low part of a
-// compensated pair is at most half an ulp of the high part, and a row's high
-// parts are at most |Z^_b| * max|v| (T^_b is a weighted sum of values whose
-// weights sum to Z^_b), so lo * S_b with S_b = 2^(25 - E), E the exponent of
-// the row's Z^ high part, stays below 4 * max|v|: within fp8 e4m3's range
-// (448) for values up to 112 in magnitude, beyond which the conversion
-// saturates and that element keeps only part of its compensation.  e4m3
-// keeps three mantissa bits of lo, so a stored low part is exact to 1/16 of
-// itself; the pair still tracks the far numerator far below one rounding of
-// the high part per token.  Rows whose Z^ is below 2^-27 (never used: Z^ >= 1
-// once a key has been absorbed) take E = -27.
-__device__ __forceinline__ uint32_t tlo_exponent(float zhi) {
-  const uint32_t e = (__float_as_uint(zhi) >> 23) & 0xffu;
-  return e < 100u ? 100u : (e > 254u ? 254u : e);
-}
-// S_b = 2^(25 - E) (encode) and 1/S_b = 2^(E - 25) (decode), exact powers of two.
-__device__ __forceinline__ float tlo_scale(float zhi) {
-  return __uint_as_float((279u - tlo_exponent(zhi)) << 23);
-}
-__device__ __forceinline__ float tlo_unscale(float zhi) {
-  return __uint_as_float((tlo_exponent(zhi) - 25u) << 23);
-}
-// Four low parts to four e4m3 bytes (x in the lowest byte), round to nearest
-// even, saturating at the largest finite value.
-__device__ __forceinline__ uint32_t tlo_pack4(float4 lo, float sc) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 l, h;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
-      "mov.b32 %0, {l, h};\n\t}"
-      : "=r"(r)
-      : "f"(lo.x * sc), "f"(lo.y * sc), "f"(lo.z * sc), "f"(lo.w * sc));
-  return r;
-}
-// Inverse of tlo_pack4: four bytes (x lowest) to four f32 low parts.
-__device__ __forceinline__ float4 tlo_unpack4(uint32_t w, float inv) {
-  float a, b, c, d;
-  asm("{\n\t.reg .b16 l, h, a0, a1, b0, b1;\n\t.reg .b32 pa, pb;\n\t"
-      "mov.b32 {l, h}, %4;\n\t"
-      "cvt.rn.f16x2.e4m3x2 pa, l;\n\t"
-      "cvt.rn.f16x2.e4m3x2 pb, h;\n\t"
-      "mov.b32 {a0, a1}, pa;\n\t"
-      "mov.b32 {b0, b1}, pb;\n\t"
-      "cvt.f32.f16 %0, a0;\n\t"
-      "cvt.f32.f16 %1, a1;\n\t"
-      "cvt.f32.f16 %2, b0;\n\t"
-      "cvt.f32.f16 %3, b1;\n\t}"
-      : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
-      : "r"(w));
-  return make_float4(a * inv, b * inv, c * inv, d * inv);
-}
 #endif
 
 // One decode token for groups [g0, g0+n): one kernel launch on `stream`.

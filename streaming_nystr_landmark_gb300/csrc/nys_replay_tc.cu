@@ -459,31 +459,20 @@ replay_tc_kernel(DevState s, int64_t g0, SealGeom sg, const float* __restrict__ 
   if (*vabort) {
     if (tid == 0) s.ints[g * kIntsPerGroup + kIntStatus] = 3;  // replay gave up
   } else {
-    // Write this CTA's rows of T^ (hi f32, lo fp8) and Z^, running maxima.
+    // Write this CTA's rows of T^ (hi f32, lo bf16) and Z^, running maxima.
     const int hh = h0 + row / m, i = row - (row / m) * m;
     const bool valid = row < heads_per_cta * m && hh < H && i < me;
     const int64_t grow = (g * H + hh) * (int64_t)m + i;
-    // Z^ lives in warpgroup 0; both column halves store their low parts at
-    // the scale it sets (every thread takes this branch: the abort flag was
-    // read after the loop's last barrier).
-    if (half == 0) alpha_s[row] = zh;
-    __syncthreads();
-    const float lsc = tlo_scale(alpha_s[row]);
     for (int c = half * cols_half; c < (half + 1) * cols_half; c += 16) {
       float hi[16], lo[16];
       tc_ld16(lane_base + kColHi + c, hi);
       tc_ld16(lane_base + kColLo + c, lo);
       if (valid) {
 #pragma unroll
-        for (int jx = 0; jx < 16; ++jx) s.t_hat[grow * dv + c + jx] = hi[jx];
-        // Sixteen fp8 low parts in one 16-byte store (dv and c are multiples
-        // of sixteen here).
-        uint4 lw;
-        lw.x = tlo_pack4(make_float4(lo[0], lo[1], lo[2], lo[3]), lsc);
-        lw.y = tlo_pack4(make_float4(lo[4], lo[5], lo[6], lo[7]), lsc);
-        lw.z = tlo_pack4(make_float4(lo[8], lo[9], lo[10], lo[11]), lsc);
-        lw.w = tlo_pack4(make_float4(lo[12], lo[13], lo[14], lo[15]), lsc);
-        *reinterpret_cast<uint4*>(s.t_lo + grow * dv + c) = lw;
+        for (int jx = 0; jx < 16; ++jx) {
+          s.t_hat[grow * dv + c + jx] = hi[jx];
+          s.t_lo[grow * dv + c + jx] = (uint16_t)(pack_bf16x2(lo[jx], 0.f) & 0xffffu);
+        }
       }
     }
     if (valid && half == 0) {

@@ -973,21 +973,14 @@ replay_kernel(DevState s, int64_t g0, SealGeom sg,
       s.z_lo[grow] = zl[i];
     }
     float* tdst = s.t_hat + grow * (int64_t)dv + c0;
-    uint8_t* ldst = s.t_lo + grow * (int64_t)dv + c0;
-    const float lsc = tlo_scale(zh[i]);
+    uint16_t* ldst = s.t_lo + grow * (int64_t)dv + c0;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int col = (c < 4 ? 0 : kValTile / 2 - 4) + tx * 4 + c;
-      if (col < cw) tdst[col] = hi[i][c];
-    }
-    // Columns come in runs of four (dv and the tile width are multiples of
-    // four): one word of four fp8 low parts per run.
-#pragma unroll
-    for (int c = 0; c < 8; c += 4) {
-      const int col = (c < 4 ? 0 : kValTile / 2 - 4) + tx * 4 + c;
-      if (col < cw)
-        *reinterpret_cast<uint32_t*>(ldst + col) = tlo_pack4(
-            make_float4(lo[i][c], lo[i][c + 1], lo[i][c + 2], lo[i][c + 3]), lsc);
+      if (col < cw) {
+        tdst[col] = hi[i][c];
+        ldst[col] = (uint16_t)(pack_bf16x2(lo[i][c], 0.f) & 0xffffu);
+      }
     }
   }
 }

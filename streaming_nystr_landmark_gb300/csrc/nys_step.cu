@@ -24,7 +24,7 @@
 //      heads; each head's T^ row is read, updated with the evicted value,
 //      written back and accumulated in the same pass, so T^ crosses HBM once
 //      each way.  Partial sums are reduced across warps in shared memory.
-// T^ and Z^ are carried as hi + lo pairs (fp32 + fp8 / fp32) updated with
+// T^ and Z^ are carried as hi + lo pairs (fp32 + bf16 / fp32) updated with
 // exact FMA product errors and two-sum, so the decode's thousands of
 // accumulations do not drift (plain f32 drifts ~1e-6 in T^ per thousand
 // tokens, which the ill-conditioned mixing row amplifies into the output).
@@ -46,7 +46,7 @@ __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
 
 // Shared-memory carve-up in floats, identical on host and device.
 struct StepSmem {
-  int q, knew, kev, vnew, vev, sig, fh, lg, rs, es, gs, zs, ms, sd, den, part;
+  int q, knew, kev, vnew, vev, sig, fh, lg, rs, es, gs, zs, ms, den, part;
   int total;
   int nrp, mp;
   __host__ __device__ StepSmem(int ht, int d, int dv, int near, int m) {
@@ -66,7 +66,6 @@ struct StepSmem {
     gs = o;   o += ht * mp;
     zs = o;   o += ht * mp;
     ms = o;   o += ht * mp;
-    sd = o;   o += ht * mp;
     den = o;  o += round4(ht);
     part = o; o += kWarps * ht * kColTile;
     total = o;
@@ -217,14 +216,11 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
       float* hzs = zs + hh * L.mp;
       float* hms = ms + hh * L.mp;
       float* hsig = sig + hh * L.nrp;
-      float* sdv = sm + L.sd + hh * L.mp;
       const int32_t fl = s.far_len[hb];
       float* zl = s.z_lo + hb * m;
       for (int i = lane; i < m_eff; i += 32) {
         const float mo = mx[i], zo = zh[i], zlo = zl[i];
         float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
-        // T^ low parts are read at the scale of Z^ before this token ...
-        sdv[i] = tlo_unscale(zo);
         if (full) {
           const float l = lg[hh * L.mp + i];
           if (l > mo) {
@@ -236,9 +232,6 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
           mx[i] = mn;
           zh[i] = zn;
           zl[i] = zln;
-          // ... and written at the scale of the updated Z^ (the landmark
-          // logit's slot is free now).
-          lg[hh * L.mp + i] = tlo_scale(zn);
         }
         rs[hh * L.mp + i] = r;
         es[hh * L.mp + i] = e;
@@ -326,10 +319,11 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
           const int64_t hb = g * H + h0 + hh;
           for (int b = warp; b < m_eff; b += kWarps) {
             float* trow = s.t_hat + (hb * m + b) * (int64_t)dv;
-            uint32_t* lrow = reinterpret_cast<uint32_t*>(s.t_lo + (hb * m + b) * (int64_t)dv);
+            uint2* lrow = reinterpret_cast<uint2*>(s.t_lo + (hb * m + b) * (int64_t)dv);
             if (cv) {
               float4 x = ld4(trow + 4 * c4);
-              float4 lo = tlo_unpack4(lrow[c4], sm[L.sd + hh * L.mp + b]);
+              const uint2 lr = lrow[c4];
+              float4 lo = make_float4(bf16_lo(lr.x), bf16_hi(lr.x), bf16_lo(lr.y), bf16_hi(lr.y));
               if (full) {
                 const float r = rs[hh * L.mp + b], e = es[hh * L.mp + b];
                 const float4 ve = ld4(vev + 4 * c4);
@@ -338,7 +332,10 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
                 kahan_axpy(x.z, lo.z, r, e, ve.z);
                 kahan_axpy(x.w, lo.w, r, e, ve.w);
                 st4(trow + 4 * c4, x);
-                lrow[c4] = tlo_pack4(lo, lg[hh * L.mp + b]);
+                uint2 lw;
+                lw.x = pack_bf16x2(lo.x, lo.y);
+                lw.y = pack_bf16x2(lo.z, lo.w);
+                lrow[c4] = lw;
               }
               const float gb = gs[hh * L.mp + b];
               acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);

@@ -17,7 +17,7 @@
 //    and the evicted key/value, running maxima, Z^), the K side (sink keys,
 //    window keys, key landmarks, each head's query landmarks, as one
 //    sequence of d-float rows), M, the V side (sink and window values), and
-//    T^ (f32 high and one-byte low rows together).  Dot products of four rows x all heads are finished with one
+//    T^ (hi and lo rows together).  Dot products of four rows x all heads are finished with one
 //    multi-value butterfly (4*HT values across 32 lanes in 4*HT - 1 shuffles).
 //
 // Every wait is bounded.  A wait that runs out sets a status word in the
@@ -299,7 +299,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         } else {
           const int r0 = (st - 1 - P.n_k - P.n_m - P.n_v) * P.rows_t;
           const int r1 = min(r0 + P.rows_t, H * m);
-          const uint32_t hb = (uint32_t)((r1 - r0) * dv * 4), lb = (uint32_t)((r1 - r0) * dv);
+          const uint32_t hb = (uint32_t)((r1 - r0) * dv * 4), lb = (uint32_t)((r1 - r0) * dv * 2);
           mbar_expect_tx(bar, hb + lb);
           bulk_load(dst, s.t_hat + (g * H * m + r0) * (int64_t)dv, hb, bar);
           bulk_load(dst + (size_t)P.rows_t * dv * 4, s.t_lo + (g * H * m + r0) * (int64_t)dv, lb,
@@ -588,9 +588,6 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             s.m_max[hb * m + i] = mn;
             s.z_hat[hb * m + i] = zn;
             s.z_lo[hb * m + i] = zln;
-            // The landmark logit is spent: its slot keeps the scale that
-            // this row's T^ low parts are stored with from now on.
-            lg[hh * P.mp + i] = tlo_scale(zn);
           }
           rs[hh * P.mp + i] = r;
           es[hh * P.mp + i] = e;
@@ -702,7 +699,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       tacc = make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float* const t_hi_g = s.t_hat + (g * H * (int64_t)m) * dv + 4 * lane;
-    uint8_t* const t_lo_g = s.t_lo + (g * H * (int64_t)m) * dv + 4 * lane;
+    uint16_t* const t_lo_g = s.t_lo + (g * H * (int64_t)m) * dv + 4 * lane;
     for (int st = 0; st < P.n_t; ++st, advance()) {
       if (!acquire_slot(ci, cpar)) { fail(g); return; }
       const unsigned char* stage = stage_ptr(ci);
@@ -717,7 +714,8 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         ++sh;
       }
       const float* hi_rows = reinterpret_cast<const float*>(stage);
-      const uint8_t* lo_rows = stage + (size_t)P.rows_t * dv * 4;
+      const uint16_t* lo_rows =
+          reinterpret_cast<const uint16_t*>(stage + (size_t)P.rows_t * dv * 4);
       const int r0 = st * P.rows_t;
       const int nrow = min(P.rows_t, H * m - r0);
 #pragma unroll (HT <= 2 ? 2 : 1)
@@ -736,14 +734,12 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         }
         if (b < m_eff && cv) {
           float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
-          // Low parts are stored relative to the row's Z^ before this token.
-          float4 lo = tlo_unpack4(
-              *reinterpret_cast<const uint32_t*>(lo_rows + (size_t)lr * dv + 4 * lane),
-              tlo_unscale(xzhi[h * m + b]));
+          const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
+          float4 lo = make_float4(bf16_lo(lr2.x), bf16_hi(lr2.x), bf16_lo(lr2.y), bf16_hi(lr2.y));
           if (full) {
             const float r = rs[h * P.mp + b], e = es[h * P.mp + b];
             float* thp;
-            uint8_t* tlp;
+            uint16_t* tlp;
             // Compensated far update (Kahan form, see kahan_axpy).
             kahan_axpy(x.x, lo.x, r, e, ve.x);
             kahan_axpy(x.y, lo.y, r, e, ve.y);
@@ -759,7 +755,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
               tlp = s.t_lo + grow * dv + 4 * lane;
             }
             st4(thp, x);
-            *reinterpret_cast<uint32_t*>(tlp) = tlo_pack4(lo, lg[h * P.mp + b]);
+            uint2 lw;
+            lw.x = pack_bf16x2(lo.x, lo.y);
+            lw.y = pack_bf16x2(lo.z, lo.w);
+            *reinterpret_cast<uint2*>(tlp) = lw;
           }
           const float gb = gs[h * P.mp + b];
           if constexpr (HT > 2) {
@@ -873,15 +872,9 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.rows_m = stage_bytes / (m * 4);
   if (P.rows_m % m) return false;  // a head's M block must not straddle stages
   P.rows_v = stage_bytes / (dv * 4);
-  // T^ rows: dv f32 high parts + dv one-byte low parts each.  The rows are
-  // spread evenly over the fewest stages, in multiples of the warp count.
-  P.rows_t = stage_bytes / (dv * 5);
+  P.rows_t = stage_bytes / (dv * 6);
+  P.rows_t &= ~1;  // keeps the bf16 block 16-byte aligned for any dv % 8 == 0
   if (P.rows_k < 1 || P.rows_m < 1 || P.rows_v < 1 || P.rows_t < 1) return false;
-  {
-    const int nt = (H * m + P.rows_t - 1) / P.rows_t;
-    const int even = ((H * m + nt - 1) / nt + kCWarps - 1) / kCWarps * kCWarps;
-    if (even < P.rows_t) P.rows_t = even;
-  }
   P.tot_k = ns + w + m + H * m;
   P.n_k = (P.tot_k + P.rows_k - 1) / P.rows_k;
   P.n_m = (H * m + P.rows_m - 1) / P.rows_m;
@@ -946,9 +939,7 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
 bool plan_step_tma(const DevState& s, void* plan_out) {
   TmaPlan& P = *static_cast<TmaPlan*>(plan_out);
   const int d = s.d, dv = s.dv, m = s.m, H = s.heads;
-  // dv % 16 == 0: a row of one-byte T^ low parts is a whole number of 16-byte
-  // units, so every bulk copy of them starts and ends on 16 bytes.
-  if (H > 8 || d > 128 || dv > 128 || (dv & 15) || (d & 3) || ((H * m) & 3) || (m & 3))
+  if (H > 8 || d > 128 || dv > 128 || (dv & 7) || (d & 3) || ((H * m) & 3) || (m & 3))
     return false;
   const int tries[4][2] = {{32768, 2}, {16384, 2}, {32768, 1}, {16384, 1}};
   for (const auto& t : tries)

@@ -40,7 +40,7 @@ def test_memory_bytes_matches_documented_layout(geo):
     cfg = nys.make_config(m, w, sink, H, d, dv, exact_cap=cap)
     sizes = [G * w * d, G * w * dv, G * sink * d, G * sink * dv, G * m * d,
              G * H * m * d, G * H * m * m, G * H * m * dv, G * H * m, G * H * m,
-             G * H * m * dv / 4, G * H * m, G * H, G * 8,   # t_lo: one byte
+             G * H * m * dv / 2, G * H * m, G * H, G * 8,   # t_lo is bf16
              G * cap * d, G * cap * dv]
     want = sum(_align(int(4 * s)) for s in sizes)
     assert nys.nys_memory_bytes(cfg, G) == want
@@ -51,7 +51,7 @@ def test_memory_line_shares_window_across_heads():
     group, so doubling the heads of a group adds only per-head bytes."""
     one = nys.nys_memory_bytes(nys.make_config(32, 128, 4, 1, 128, 128), 1)
     two = nys.nys_memory_bytes(nys.make_config(32, 128, 4, 2, 128, 128), 1)
-    per_head = 4 * (32 * 128 + 32 * 32 + 32 * 128 + 2 * 32 + 1) + 32 * 128 + 4 * 32
+    per_head = 4 * (32 * 128 + 32 * 32 + 32 * 128 + 2 * 32 + 1) + 2 * 32 * 128 + 4 * 32
     assert abs((two - one) - per_head) <= 256 * 8
     assert two < 2 * one
 

@@ -1,8 +1,9 @@
-"""The one-byte low part of the far numerator does its job.
+"""The low part of the far numerator does its job.
 
 The state comparisons in the parity tests bound T^ at 1e-5 relative, far
 above one f32 rounding, so they cannot tell a working low part from a broken
-one (wrong byte order, wrong scale).  Two checks that can:
+one (a low part stored in the wrong half of its word, or dropped).  Two
+checks that can:
 
 * Closed form.  With every prompt query zero, every query landmark is zero,
   every far logit is exactly 0 and every far weight exactly 1 (the running
@@ -64,14 +65,13 @@ def test_decode_low_part_tracks_exact_sums(cuda_device, heads, d, dv):
     err_hi = np.abs(hi - ref[:, None, None, :])
     err_full = np.abs(full - ref[:, None, None, :])
     # Each token's addition rounds hi by up to half an ulp and leaves the
-    # residual in lo; lo is stored to 1/16 of itself at every token, and
-    # those storage errors accumulate.  A CPU emulation of this scenario
-    # gives err_full ~0.36 err_hi on average; a lost, mis-scaled or
-    # scrambled low part gives ~1 or more.
-    assert err_full.mean() < 0.6 * err_hi.mean(), (err_hi.mean(), err_full.mean())
-    # Normwise, no element strays past one ulp of its row's largest sum.
+    # residual in lo; lo is stored as bf16 (eight significant bits) at every
+    # token, and those storage errors accumulate.  A CPU emulation of this
+    # scenario gives err_full ~0.04 err_hi on average and at most ~0.02 ulp
+    # of the row's largest sum; a lost or scrambled low part gives ~1 or more.
+    assert err_full.mean() < 0.2 * err_hi.mean(), (err_hi.mean(), err_full.mean())
     row_ulp = _ulp(np.abs(ref).max(axis=1))[:, None, None, None]
-    assert np.all(err_full <= row_ulp), float((err_full / row_ulp).max())
+    assert np.all(err_full <= 0.25 * row_ulp), float((err_full / row_ulp).max())
     st.close()
 
 
