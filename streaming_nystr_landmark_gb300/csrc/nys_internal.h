@@ -111,6 +111,41 @@ __device__ __forceinline__ void kahan_axpy(float& hi, float& lo, float r, float 
   hi = t;
 }
 
+// kahan_axpy on four elements sharing r and e (one T^ row chunk): the rescale
+// test is taken once for the four, then each element gets the same
+// operations in the same order as kahan_axpy.
+__device__ __forceinline__ void kahan_axpy4(float4& hi, float4& lo, float r, float e, float4 v) {
+  if (r != 1.f) {
+    float a = hi.x * r;
+    lo.x = fmaf(lo.x, r, fmaf(hi.x, r, -a));
+    hi.x = a;
+    a = hi.y * r;
+    lo.y = fmaf(lo.y, r, fmaf(hi.y, r, -a));
+    hi.y = a;
+    a = hi.z * r;
+    lo.z = fmaf(lo.z, r, fmaf(hi.z, r, -a));
+    hi.z = a;
+    a = hi.w * r;
+    lo.w = fmaf(lo.w, r, fmaf(hi.w, r, -a));
+    hi.w = a;
+  }
+  float yv = fmaf(e, v.x, lo.x), t = hi.x + yv;
+  lo.x = yv - (t - hi.x);
+  hi.x = t;
+  yv = fmaf(e, v.y, lo.y);
+  t = hi.y + yv;
+  lo.y = yv - (t - hi.y);
+  hi.y = t;
+  yv = fmaf(e, v.z, lo.z);
+  t = hi.z + yv;
+  lo.z = yv - (t - hi.z);
+  hi.z = t;
+  yv = fmaf(e, v.w, lo.w);
+  t = hi.w + yv;
+  lo.w = yv - (t - hi.w);
+  hi.w = t;
+}
+
 // comp_axpy with r == 1, for callers that branch on r once for many elements.
 __device__ __forceinline__ void comp_add(float hi, float lo, float x, float y, float& nhi,
                                          float& nlo) {
@@ -160,6 +195,39 @@ __device__ __forceinline__ float dot2(const float* x, const float* y, int ys, in
     c0 += ((s0 - (t - z)) + (h - z)) + r;
     s0 = t;
   }
+  const float t = s0 + s1;
+  const float z = t - s0;
+  const float e = (s0 - (t - z)) + (s1 - z);
+  return t + ((c0 + c1) + e);
+}
+
+// dot2 with x read four at a time (x 16-byte aligned): the same operations
+// in the same order -- even terms on the first chain, odd on the second --
+// so the result is bit-identical to dot2's.
+__device__ __forceinline__ float dot2_x4(const float* x, const float* y, int ys, int n) {
+  float s0 = 0.f, c0 = 0.f, s1 = 0.f, c1 = 0.f;
+  auto term = [](float& sv, float& cv, float xa, float ya) {
+    const float h = xa * ya;
+    const float r = fmaf(xa, ya, -h);
+    const float t = sv + h;
+    const float z = t - sv;
+    cv += ((sv - (t - z)) + (h - z)) + r;
+    sv = t;
+  };
+  int a = 0;
+  for (; a + 4 <= n; a += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(x + a);
+    term(s0, c0, xv.x, y[a * ys]);
+    term(s1, c1, xv.y, y[(a + 1) * ys]);
+    term(s0, c0, xv.z, y[(a + 2) * ys]);
+    term(s1, c1, xv.w, y[(a + 3) * ys]);
+  }
+  if (a + 2 <= n) {
+    term(s0, c0, x[a], y[a * ys]);
+    term(s1, c1, x[a + 1], y[(a + 1) * ys]);
+    a += 2;
+  }
+  if (a < n) term(s0, c0, x[a], y[a * ys]);
   const float t = s0 + s1;
   const float z = t - s0;
   const float e = (s0 - (t - z)) + (s1 - z);

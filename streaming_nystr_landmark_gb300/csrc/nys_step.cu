@@ -255,7 +255,7 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
         const float* M = s.mu + hb * m * (int64_t)m;
         float cm = -INFINITY;
         for (int b = lane; b < m_eff; b += 32) {
-          float u = dot2(hfh, M + b, m, m_eff);
+          float u = dot2_x4(hfh, M + b, m, m_eff);
           if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
           hgs[b] = u;
           cm = fmaxf(cm, f + hms[b]);
@@ -326,22 +326,19 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
               float4 lo = make_float4(bf16_lo(lr.x), bf16_hi(lr.x), bf16_lo(lr.y), bf16_hi(lr.y));
               if (full) {
                 const float r = rs[hh * L.mp + b], e = es[hh * L.mp + b];
-                const float4 ve = ld4(vev + 4 * c4);
-                kahan_axpy(x.x, lo.x, r, e, ve.x);
-                kahan_axpy(x.y, lo.y, r, e, ve.y);
-                kahan_axpy(x.z, lo.z, r, e, ve.z);
-                kahan_axpy(x.w, lo.w, r, e, ve.w);
+                kahan_axpy4(x, lo, r, e, ld4(vev + 4 * c4));
                 st4(trow + 4 * c4, x);
                 uint2 lw;
                 lw.x = pack_bf16x2(lo.x, lo.y);
                 lw.y = pack_bf16x2(lo.z, lo.w);
                 lrow[c4] = lw;
               }
+              // High part only: the low part is under half an ulp of it.
               const float gb = gs[hh * L.mp + b];
-              acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
-              acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
-              acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
-              acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
+              acc[hh].x = fmaf(gb, x.x, acc[hh].x);
+              acc[hh].y = fmaf(gb, x.y, acc[hh].y);
+              acc[hh].z = fmaf(gb, x.z, acc[hh].z);
+              acc[hh].w = fmaf(gb, x.w, acc[hh].w);
             }
           }
         }

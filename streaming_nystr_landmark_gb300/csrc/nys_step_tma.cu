@@ -55,7 +55,7 @@ struct TmaPlan {
   int misc_bytes;
   // consumer scratch (floats, after the ring)
   int x_q, x_knew, x_vnew, x_kev, x_vev, x_mmax, x_zhi, x_zlo;
-  int x_sig, x_fh, x_lg, x_rs, x_es, x_gs, x_zs, x_ms, x_den, x_fl, x_ints, x_part;
+  int x_sig, x_fh, x_lg, x_rc, x_ms, x_den, x_fl, x_ints, x_part;
   int nrp, mp, scratch_floats;
   int ring;
   int debug_skip;   // test hook: ring stage CTA 0 withholds (-1: none)
@@ -323,6 +323,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
 
   // ============================================================ consumers
   float* xq = X + P.x_q;
+  float* pT = xq;  // near weights [sink + window row][HT], written by the per-head phase
   float* xknew = X + P.x_knew;
   float* xvnew = X + P.x_vnew;
   float* xkev = X + P.x_kev;
@@ -333,10 +334,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   float* sig = X + P.x_sig;
   float* fh = X + P.x_fh;
   float* lg = X + P.x_lg;
-  float* rs = X + P.x_rs;
-  float* es = X + P.x_es;
-  float* gs = X + P.x_gs;
-  float* zs = X + P.x_zs;
+  // Per (head, landmark): {rescale r, weight e of the evicted key, gain g,
+  // updated Z^ (hi + lo)}, one 16-byte load per T^ row.
+  float4* rc = reinterpret_cast<float4*>(X + P.x_rc);
   float* ms = X + P.x_ms;
   float* den = X + P.x_den;
   int* xints = reinterpret_cast<int*>(X + P.x_ints);
@@ -566,8 +566,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         if (hh < h_lo || hh >= h_hi) continue;
         const int64_t hb = g * H + hh;
         float* hfh = fh + hh * P.mp;
-        float* hgs = gs + hh * P.mp;
-        float* hzs = zs + hh * P.mp;
+        float4* hrc = rc + hh * P.mp;
         float* hms = ms + hh * P.mp;
         float* hsig = sig + hh * P.nrp;
         // (1) Landmark updates: delayed insertion of the evicted key with
@@ -589,9 +588,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
             s.z_hat[hb * m + i] = zn;
             s.z_lo[hb * m + i] = zln;
           }
-          rs[hh * P.mp + i] = r;
-          es[hh * P.mp + i] = e;
-          hzs[i] = zn + zln;
+          hrc[i] = make_float4(r, e, 0.f, zn + zln);
           hms[i] = mn;
           mx_m = fmaxf(mx_m, mn);
         }
@@ -613,7 +610,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         float psum = 0.f;
         for (int j = lane; j < nnear; j += 32) {
           const float p = expf(hsig[j] - c_all);
-          hsig[j] = p;
+          pT[j * HT + hh] = p;
           psum += p;
         }
         // (4) Far mix u = F^ M (rectified), weights g_b on the joint scale,
@@ -625,21 +622,21 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           const float* Mh = reinterpret_cast<const float*>(stage_ptr(ci)) +
                             (size_t)(hh - h_lo) * m * m;
           for (int b = lane; b < m_eff; b += 32) {
-            float u = dot2(hfh, Mh + b, m, m_eff);
+            float u = dot2_x4(hfh, Mh + b, m, m_eff);
             if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
             const float gb = u * expf(f + hms[b] - c_all);
-            hgs[b] = gb;
-            acc = fmaf(gb, hzs[b], acc);
+            hrc[b].z = gb;
+            acc = fmaf(gb, hrc[b].w, acc);
           }
         } else {
-          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+          for (int b = lane; b < m_eff; b += 32) hrc[b].z = 0.f;
         }
         warp_sum2(acc, psum);
         float far_den = has_far ? acc : 0.f;
         // Guard: a negative (or NaN) far denominator drops the far field.
         if (has_far && !(far_den >= 0.f)) {
           far_den = 0.f;
-          for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;
+          for (int b = lane; b < m_eff; b += 32) hrc[b].z = 0.f;
         }
         if (lane == 0) den[hh] = fmaxf(far_den + psum, 1e-30f);
       }
@@ -665,9 +662,28 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         if (j < nnear && cv) {
           const float* row = (j - ns == slot) ? xvnew : stage + (size_t)lr * dv;
           const float4 a = ld4(row + 4 * lane);
+          // This row's weight for every head (slots past H hold stale values
+          // and feed accumulators that are never written out).
+          float pw[HT];
+          if constexpr (HT % 4 == 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < HT / 4; ++q4) {
+              const float4 t = ld4(pT + j * HT + 4 * q4);
+              pw[4 * q4] = t.x;
+              pw[4 * q4 + 1] = t.y;
+              pw[4 * q4 + 2] = t.z;
+              pw[4 * q4 + 3] = t.w;
+            }
+          } else if constexpr (HT == 2) {
+            const float2 t = *reinterpret_cast<const float2*>(pT + j * 2);
+            pw[0] = t.x;
+            pw[1] = t.y;
+          } else {
+            pw[0] = pT[j];
+          }
 #pragma unroll
           for (int hh = 0; hh < HT; ++hh) {
-            const float p = (hh < H) ? sig[hh * P.nrp + j] : 0.f;
+            const float p = pw[hh];
             acc[hh].x = fmaf(p, a.x, acc[hh].x);
             acc[hh].y = fmaf(p, a.y, acc[hh].y);
             acc[hh].z = fmaf(p, a.z, acc[hh].z);
@@ -736,44 +752,34 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
           const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
           float4 lo = make_float4(bf16_lo(lr2.x), bf16_hi(lr2.x), bf16_lo(lr2.y), bf16_hi(lr2.y));
+          const float4 cf = rc[h * P.mp + b];  // {r, e, g, Z^}
           if (full) {
-            const float r = rs[h * P.mp + b], e = es[h * P.mp + b];
-            float* thp;
-            uint16_t* tlp;
-            // Compensated far update (Kahan form, see kahan_axpy).
-            kahan_axpy(x.x, lo.x, r, e, ve.x);
-            kahan_axpy(x.y, lo.y, r, e, ve.y);
-            kahan_axpy(x.z, lo.z, r, e, ve.z);
-            kahan_axpy(x.w, lo.w, r, e, ve.w);
-            if constexpr (HT > 2) {
-              const int row = r0 + lr;  // = h * m + b
-              thp = t_hi_g + (size_t)row * dv;
-              tlp = t_lo_g + (size_t)row * dv;
-            } else {
-              const int64_t grow = (g * H + h) * (int64_t)m + b;
-              thp = s.t_hat + grow * dv + 4 * lane;
-              tlp = s.t_lo + grow * dv + 4 * lane;
-            }
-            st4(thp, x);
+            // Compensated far update (Kahan form), written back in place:
+            // the group's T^ rows are h * m + b = r0 + lr.
+            kahan_axpy4(x, lo, cf.x, cf.y, ve);
+            const size_t ro = (size_t)(r0 + lr) * dv;
+            st4(t_hi_g + ro, x);
             uint2 lw;
             lw.x = pack_bf16x2(lo.x, lo.y);
             lw.y = pack_bf16x2(lo.z, lo.w);
-            *reinterpret_cast<uint2*>(tlp) = lw;
+            *reinterpret_cast<uint2*>(t_lo_g + ro) = lw;
           }
-          const float gb = gs[h * P.mp + b];
+          // The far numerator enters the output through its high part: the
+          // low part is under half an ulp of it, as small as the contraction's
+          // own rounding; it matters only for the state it carries forward.
           if constexpr (HT > 2) {
-            tacc.x = fmaf(gb, x.x + lo.x, tacc.x);
-            tacc.y = fmaf(gb, x.y + lo.y, tacc.y);
-            tacc.z = fmaf(gb, x.z + lo.z, tacc.z);
-            tacc.w = fmaf(gb, x.w + lo.w, tacc.w);
+            tacc.x = fmaf(cf.z, x.x, tacc.x);
+            tacc.y = fmaf(cf.z, x.y, tacc.y);
+            tacc.z = fmaf(cf.z, x.z, tacc.z);
+            tacc.w = fmaf(cf.z, x.w, tacc.w);
           } else {
 #pragma unroll
             for (int hh = 0; hh < HT; ++hh) {
               if (hh == h) {
-                acc[hh].x = fmaf(gb, x.x + lo.x, acc[hh].x);
-                acc[hh].y = fmaf(gb, x.y + lo.y, acc[hh].y);
-                acc[hh].z = fmaf(gb, x.z + lo.z, acc[hh].z);
-                acc[hh].w = fmaf(gb, x.w + lo.w, acc[hh].w);
+                acc[hh].x = fmaf(cf.z, x.x, acc[hh].x);
+                acc[hh].y = fmaf(cf.z, x.y, acc[hh].y);
+                acc[hh].z = fmaf(cf.z, x.z, acc[hh].z);
+                acc[hh].w = fmaf(cf.z, x.w, acc[hh].w);
               }
             }
           }
@@ -896,7 +902,9 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.nrp = r4(ns + w);
   P.mp = r4(m);
   int x = 0;
-  P.x_q = x;    x += ht * d;
+  // The queries are read once, into registers, at the start of the K side;
+  // afterwards the region holds the near weights transposed, [row][head].
+  P.x_q = x;    x += (ht * d > P.nrp * ht) ? ht * d : P.nrp * ht;
   P.x_knew = x; x += d;
   P.x_vnew = x; x += dv;
   P.x_kev = x;  x += d;
@@ -907,10 +915,7 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.x_sig = x;  x += ht * P.nrp;
   P.x_fh = x;   x += ht * P.mp;
   P.x_lg = x;   x += ht * P.mp;
-  P.x_rs = x;   x += ht * P.mp;
-  P.x_es = x;   x += ht * P.mp;
-  P.x_gs = x;   x += ht * P.mp;
-  P.x_zs = x;   x += ht * P.mp;
+  P.x_rc = x;   x += 4 * ht * P.mp;  // float4 per (head, landmark); x stays a multiple of 4
   P.x_ms = x;   x += ht * P.mp;
   P.x_den = x;  x += r4(ht);
   P.x_fl = x;   x += r4(ht);
