@@ -324,8 +324,13 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
   // ============================================================ consumers
   float* xq = X + P.x_q;
   float* pT = xq;  // near weights [sink + window row][HT], written by the per-head phase
-  float* xknew = X + P.x_knew;
-  float* xvnew = X + P.x_vnew;
+  // The new key and value alternate between two buffers from group to
+  // group: the ring-slot write at the end of a group reads them while a
+  // faster warp may already copy the next group's in, so no barrier is
+  // needed between the two.
+  float* const xknew2 = X + P.x_knew;
+  float* const xvnew2 = X + P.x_vnew;
+  int nbuf = 0;
   float* xkev = X + P.x_kev;
   float* xvev = X + P.x_vev;
   float* xmmax = X + P.x_mmax;
@@ -377,8 +382,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         s.ints[g2 * kIntsPerGroup + kIntStatus] = 1;
   };
 
-  for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x) {
+  for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x, nbuf ^= 1) {
     const int64_t g = g0 + gi;
+    float* const xknew = xknew2 + nbuf * d;
+    float* const xvnew = xvnew2 + nbuf * dv;
     // far_len of the head this warp owns in the per-head phase; loaded now so
     // that its latency hides behind the K side.
     const int fl_old = (warp < H && lane == 0) ? s.far_len[g * H + warp] : 0;
@@ -788,28 +795,38 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       release_slot(ci);
     }
     if constexpr (HT > 2) flush_far();
-    // Cross-warp sum in two rounds through a buffer of kCWarps/2 slots.
-    constexpr int kHalf = kCWarps / 2;
-    if (warp >= kHalf && cv) {
+    // Cross-warp sum of the output numerators.  With up to two heads every
+    // warp's partials fit the buffer: one barrier, then each output sums
+    // kCWarps partials.  With more heads, two rounds through kCWarps/2 slots.
+    constexpr int kSlots = HT <= 2 ? kCWarps : kCWarps / 2;
+    if constexpr (HT <= 2) {
+      if (cv) {
 #pragma unroll
-      for (int hh = 0; hh < HT; ++hh)
-        st4(part + ((warp - kHalf) * HT + hh) * 128 + 4 * lane, acc[hh]);
-    }
-    if (!csync()) { fail(g); return; }
-    if (warp < kHalf && cv) {
-#pragma unroll
-      for (int hh = 0; hh < HT; ++hh) {
-        float* p = part + (warp * HT + hh) * 128 + 4 * lane;
-        const float4 o = ld4(p);
-        st4(p, make_float4(o.x + acc[hh].x, o.y + acc[hh].y, o.z + acc[hh].z, o.w + acc[hh].w));
+        for (int hh = 0; hh < HT; ++hh) st4(part + (warp * HT + hh) * 128 + 4 * lane, acc[hh]);
       }
+      if (!csync()) { fail(g); return; }
+    } else {
+      if (warp >= kSlots && cv) {
+#pragma unroll
+        for (int hh = 0; hh < HT; ++hh)
+          st4(part + ((warp - kSlots) * HT + hh) * 128 + 4 * lane, acc[hh]);
+      }
+      if (!csync()) { fail(g); return; }
+      if (warp < kSlots && cv) {
+#pragma unroll
+        for (int hh = 0; hh < HT; ++hh) {
+          float* p = part + (warp * HT + hh) * 128 + 4 * lane;
+          const float4 o = ld4(p);
+          st4(p, make_float4(o.x + acc[hh].x, o.y + acc[hh].y, o.z + acc[hh].z, o.w + acc[hh].w));
+        }
+      }
+      if (!csync()) { fail(g); return; }
     }
-    if (!csync()) { fail(g); return; }
     for (int idx = tid; idx < H * dv; idx += kCThreads) {
       const int hh = idx / dv, col = idx - hh * dv;
       float sum = 0.f;
 #pragma unroll
-      for (int wp = 0; wp < kHalf; ++wp) sum += part[(wp * HT + hh) * 128 + col];
+      for (int wp = 0; wp < kSlots; ++wp) sum += part[(wp * HT + hh) * 128 + col];
       out[(gi * H + hh) * (int64_t)dv + col] = sum / den[hh];
     }
     // The ring slot takes the new key/value; the counters move on.
@@ -822,7 +839,9 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       if (full) ints[kIntWinHead] = (win_head + 1) % w;
       else ints[kIntWinLen] = win_len + 1;
     }
-    if (!csync()) { fail(g); return; }
+    // No barrier here: the next group's misc copy writes the other new
+    // key/value buffer, and every other scratch value read above (the
+    // partials, den) is next written after that group's first barriers.
   }
 }
 
@@ -905,8 +924,8 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   // The queries are read once, into registers, at the start of the K side;
   // afterwards the region holds the near weights transposed, [row][head].
   P.x_q = x;    x += (ht * d > P.nrp * ht) ? ht * d : P.nrp * ht;
-  P.x_knew = x; x += d;
-  P.x_vnew = x; x += dv;
+  P.x_knew = x; x += 2 * d;   // two buffers, used by alternate groups
+  P.x_vnew = x; x += 2 * dv;
   P.x_kev = x;  x += d;
   P.x_vev = x;  x += dv;
   P.x_mmax = x; x += H * m;
@@ -920,7 +939,7 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.x_den = x;  x += r4(ht);
   P.x_fl = x;   x += r4(ht);
   P.x_ints = x; x += kIntsPerGroup;
-  P.x_part = x; x += (kCWarps / 2) * ht * 128;
+  P.x_part = x; x += (ht <= 2 ? kCWarps : kCWarps / 2) * ht * 128;
   P.scratch_floats = x;
   P.ring_off = 1024;  // barriers and the abort flag live below
   const long budget = per_sm == 2 ? kSmemBudget2 : kSmemBudget;

@@ -58,17 +58,23 @@ def test_sweep_workload_full_size(cuda_device, m, rect):
 
 def test_batch64_workload_full_size(cuda_device):
     """64 seq x 28 layers x 8 groups = 14336 groups per launch, t=256, all
-    1024 tokens; 4 groups spread over sequences and layers checked."""
+    1024 tokens; 8 groups checked: spread over sequences and layers, and
+    the first, second and last groups of the launch's first CTA (the
+    persistent kernel's 304 CTAs take groups c, c + 304, ...)."""
     wl = WORKLOADS["batch64"]
-    _run(wl, [0, 8 * 28 * 17 + 8 * 5 + 3, 8 * 28 * 40 + 7, wl.n_groups - 1],
+    _run(wl, [0, 1, 304, 608, 8 * 28 * 17 + 8 * 5 + 3, 8 * 28 * 40 + 7,
+              wl.n_groups - 304, wl.n_groups - 1],
          cuda_device, check_every=256)
 
 
 def test_long_context_workload_full_size(cuda_device):
     """512 groups x 8 heads, m=64, t=32768 (sealed in one call), 2048
-    tokens; one group checked against the oracle's sequential replay."""
+    tokens; four groups checked against the oracle's sequential replay: the
+    eight-head kernel runs 256 CTAs of two groups (c and c + 256), so
+    groups 0 and 256 are one CTA's first and second, 131 and 509 two
+    others'."""
     wl = WORKLOADS["long"]
-    _run(wl, [wl.n_groups - 3], cuda_device, check_every=512)
+    _run(wl, [0, 131, 256, wl.n_groups - 3], cuda_device, check_every=512)
 
 
 @pytest.mark.parametrize("geo", [
