@@ -560,66 +560,75 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     }
     if (!csync()) { fail(g); return; }
 
-    // ---- B: per-head scalars.  M streams through the ring a stage at a time
-    // (each stage holds the blocks of heads_per_stage consecutive heads); a
-    // head's warp works as soon as its block has landed and every stage is
-    // handed back right after, so the ring never has to hold all of M.
+    // ---- B: per-head scalars, one warp per head (H <= kCWarps, so a warp
+    // has at most one).  Steps (1)-(3) need no M and run first, while M is
+    // still on its way; then M streams through the ring a stage at a time
+    // (each stage holds the blocks of heads_per_stage consecutive heads), a
+    // head's warp takes step (4) as soon as its block has landed, and every
+    // stage is handed back right after, so the ring never holds all of M.
+    const int hh = warp;
+    float c_all = 0.f, f = 0.f, psum = 0.f;
+    bool has_far = false;
+    if (hh < H) {
+      const int64_t hb = g * H + hh;
+      float* hfh = fh + hh * P.mp;
+      float4* hrc = rc + hh * P.mp;
+      float* hms = ms + hh * P.mp;
+      float* hsig = sig + hh * P.nrp;
+      // (1) Landmark updates: delayed insertion of the evicted key with the
+      //     running-maximum rescale.  mx_m collects the maximum of the new
+      //     running maxima.
+      float mx_m = -INFINITY;
+      for (int i = lane; i < m_eff; i += 32) {
+        const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
+        float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
+        if (full) {
+          const float l = lg[hh * P.mp + i];
+          if (l > mo) {
+            r = expf(mo - l);
+            mn = l;
+          }
+          e = expf(l - mn);
+          comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
+          s.m_max[hb * m + i] = mn;
+          s.z_hat[hb * m + i] = zn;
+          s.z_lo[hb * m + i] = zln;
+        }
+        hrc[i] = make_float4(r, e, 0.f, zn + zln);
+        hms[i] = mn;
+        mx_m = fmaxf(mx_m, mn);
+      }
+      const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
+      if (full && lane == 0) s.far_len[hb] = fl_new;
+      has_far = fl_new > 0;
+      // (2) The maxima: near logits, landmark logits f, and the running
+      //     maxima, reduced together.  max_b (f + m_b) = f + max_b m_b
+      //     exactly, since rounding is monotonic.
+      float cmax = -INFINITY;
+      f = -INFINITY;
+      for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
+      if (has_far)
+        for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
+      warp_max3(cmax, f, mx_m);
+      c_all = has_far ? fmaxf(cmax, f + mx_m) : cmax;
+      if (has_far)
+        for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
+      // (3) Near weights on the joint scale.
+      for (int j = lane; j < nnear; j += 32) {
+        const float p = expf(hsig[j] - c_all);
+        pT[j * HT + hh] = p;
+        psum += p;
+      }
+    }
     const int heads_per_stage = P.rows_m / m;
     for (int mst = 0; mst < P.n_m; ++mst, advance()) {
       if (!acquire_slot(ci, cpar)) { fail(g); return; }
       const int h_lo = mst * heads_per_stage;
       const int h_hi = min(H, h_lo + heads_per_stage);
-      for (int hh = warp; hh < H; hh += kCWarps) {
-        if (hh < h_lo || hh >= h_hi) continue;
-        const int64_t hb = g * H + hh;
-        float* hfh = fh + hh * P.mp;
+      if (hh < H && hh >= h_lo && hh < h_hi) {
         float4* hrc = rc + hh * P.mp;
+        float* hfh = fh + hh * P.mp;
         float* hms = ms + hh * P.mp;
-        float* hsig = sig + hh * P.nrp;
-        // (1) Landmark updates: delayed insertion of the evicted key with
-        //     the running-maximum rescale.  mx_m collects the maximum of the
-        //     new running maxima.
-        float mx_m = -INFINITY;
-        for (int i = lane; i < m_eff; i += 32) {
-          const float mo = xmmax[hh * m + i], zo = xzhi[hh * m + i], zlo = xzlo[hh * m + i];
-          float r = 1.f, e = 0.f, mn = mo, zn = zo, zln = zlo;
-          if (full) {
-            const float l = lg[hh * P.mp + i];
-            if (l > mo) {
-              r = expf(mo - l);
-              mn = l;
-            }
-            e = expf(l - mn);
-            comp_axpy(zo, zlo, r, e, 1.f, zn, zln);
-            s.m_max[hb * m + i] = mn;
-            s.z_hat[hb * m + i] = zn;
-            s.z_lo[hb * m + i] = zln;
-          }
-          hrc[i] = make_float4(r, e, 0.f, zn + zln);
-          hms[i] = mn;
-          mx_m = fmaxf(mx_m, mn);
-        }
-        const int fl_new = __shfl_sync(0xffffffffu, fl_old, 0) + (full ? 1 : 0);
-        if (full && lane == 0) s.far_len[hb] = fl_new;
-        const bool has_far = fl_new > 0;
-        // (2) The maxima: near logits, landmark logits f, and the running
-        //     maxima, reduced together.  max_b (f + m_b) = f + max_b m_b
-        //     exactly, since rounding is monotonic.
-        float cmax = -INFINITY, f = -INFINITY;
-        for (int j = lane; j < nnear; j += 32) cmax = fmaxf(cmax, hsig[j]);
-        if (has_far)
-          for (int a = lane; a < m_eff; a += 32) f = fmaxf(f, hfh[a]);
-        warp_max3(cmax, f, mx_m);
-        const float c_all = has_far ? fmaxf(cmax, f + mx_m) : cmax;
-        if (has_far)
-          for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
-        // (3) Near weights on the joint scale.
-        float psum = 0.f;
-        for (int j = lane; j < nnear; j += 32) {
-          const float p = expf(hsig[j] - c_all);
-          pT[j * HT + hh] = p;
-          psum += p;
-        }
         // (4) Far mix u = F^ M (rectified), weights g_b on the joint scale,
         //     far denominator; both sums reduced together.
         float acc = 0.f;
@@ -899,6 +908,9 @@ static bool plan_with(const DevState& s, int stage_bytes, int per_sm, TmaPlan& P
   P.rows_v = stage_bytes / (dv * 4);
   P.rows_t = stage_bytes / (dv * 6);
   P.rows_t &= ~1;  // keeps the bf16 block 16-byte aligned for any dv % 8 == 0
+  // A whole number of rows per consumer warp in every full stage (measured:
+  // batch64 0.6449 -> 0.6415 ms, the eight-head decode 0.1346 -> 0.1339).
+  if (P.rows_t >= kCWarps) P.rows_t -= P.rows_t % kCWarps;
   if (P.rows_k < 1 || P.rows_m < 1 || P.rows_v < 1 || P.rows_t < 1) return false;
   P.tot_k = ns + w + m + H * m;
   P.n_k = (P.tot_k + P.rows_k - 1) / P.rows_k;
