@@ -273,11 +273,14 @@ def run_reference(args, wl):
     if rank != 0:
         return
     cores = host_cores()
-    groups = oracle_groups(wl, cores * max(1, args.ref_groups))
+    # Enough groups per core that every process times >= ~256 group-steps
+    # even for a small --steps (short windows are dominated by start skew).
+    per_core = min(32, max(args.ref_groups, -(-256 // max(args.steps, 1))))
+    groups = oracle_groups(wl, cores * per_core)
     gs, dt, done = time_oracle(wl, groups, args.steps, args.warmup,
                                budget_s=args.ref_budget, procs=cores)
     value = gs / dt
-    sample = (f"{len(groups)} of {wl.n_groups} groups ({args.ref_groups} per "
+    sample = (f"{len(groups)} of {wl.n_groups} groups ({per_core} per "
               f"core), sealed untimed on the t={wl.t} prompt, then "
               f"{args.warmup} untimed + at least {done} timed decode tokens "
               f"each (at most {args.steps}, {args.ref_budget:.0f} s budget); "
