@@ -458,10 +458,115 @@ def run_ours(args, wl):
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if world == 1 and not args.no_secondary:
+        # Driver-visible figures of two other paths (not part of `value`).
+        line["secondary"] = {"long_decode": secondary_long_decode(dev),
+                             "per_layer_graph": secondary_layers_graph(dev)}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def secondary_long_decode(dev, steps=300, warmup=5):
+    """The eight-head long-context decode (512 groups: 128 sequences x 4 KV
+    heads, H=8, m=64, d=128), timed like the main line.  The decode state's
+    shape and byte count do not depend on the prompt length once m_eff = m,
+    so a 1024-token prompt stands in for the 32K one (the seal of the full
+    prompt is timed by --mode seal --workload long)."""
+    import torch
+    from streaming_nystr_landmark_gb300.nys import NystromStates
+    from streaming_nystr_landmark_gb300.workloads import WORKLOADS, DeviceFill
+    wl = WORKLOADS["long"].with_(t=1024)
+    G, H = wl.n_groups, wl.heads_per_kv
+    st = NystromStates(wl.m, wl.w, wl.sink, H, wl.d, wl.dv, G, wl.rect, dev)
+    fill = DeviceFill(wl, dev, seed=3000)
+    q = torch.empty((G, H, wl.t, wl.d), device=dev)
+    k = torch.empty((G, wl.t, wl.d), device=dev)
+    v = torch.empty((G, wl.t, wl.dv), device=dev)
+    fill.prompt_into(q, k, v)
+    st.seal(q, k, v)
+    del q, k, v
+    pool = 64
+    tq = torch.empty((pool, G, H, wl.d), device=dev)
+    tk = torch.empty((pool, G, wl.d), device=dev)
+    tv = torch.empty((pool, G, wl.dv), device=dev)
+    fill.tokens_into(tq, tk, tv)
+    out = torch.empty((G, H, wl.dv), device=dev)
+    for i in range(warmup):
+        st.step(tq[i % pool], tk[i % pool], tv[i % pool], out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for i in range(steps):
+        st.step(tq[i % pool], tk[i % pool], tv[i % pool], out)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    st.close()
+    ms = e0.elapsed_time(e1) / steps
+    peak, _ = measured_peak()
+    alg, over = algorithmic_bytes(wl), state_overhead_bytes(wl)
+    return {"workload": ("long decode: 128 seq x 4 KV groups = 512 group states, "
+                         "heads_per_kv=8, d=dv=128, m=64, w=128, sink=4 (1024-token "
+                         "prompt: same decode state as the 32K one)"),
+            "steps": steps, "ms_per_step": ms, "group_steps_per_s": G / (ms / 1e3),
+            "frac": alg * G / (ms / 1e3) / 1e9 / peak,
+            "frac_incl_state_overhead": (alg + over) * G / (ms / 1e3) / 1e9 / peak}
+
+
+def secondary_layers_graph(dev, reps=25):
+    """batch64 decoded as a model runs it: 28 per-layer handles (512 groups
+    each), one launch per layer per token, 8 tokens per CUDA graph replay."""
+    import torch
+    from streaming_nystr_landmark_gb300.nys import NystromStates
+    from streaming_nystr_landmark_gb300.workloads import WORKLOADS, DeviceFill
+    wl = WORKLOADS["batch64"]
+    L, H, per = wl.layers, wl.heads_per_kv, wl.seqs * wl.kv_groups
+    fill = DeviceFill(wl.with_(layers=1), dev, seed=4000)
+    layers = []
+    for _ in range(L):
+        st = NystromStates(wl.m, wl.w, wl.sink, H, wl.d, wl.dv, per, wl.rect, dev)
+        q = torch.empty((per, H, wl.t, wl.d), device=dev)
+        k = torch.empty((per, wl.t, wl.d), device=dev)
+        v = torch.empty((per, wl.t, wl.dv), device=dev)
+        fill.prompt_into(q, k, v)
+        st.seal(q, k, v)
+        layers.append(st)
+        del q, k, v
+    T = 8
+    tq = torch.empty((T, L, per, H, wl.d), device=dev)
+    tk = torch.empty((T, L, per, wl.d), device=dev)
+    tv = torch.empty((T, L, per, wl.dv), device=dev)
+    for i in range(T):
+        fill.tokens_into(tq[i], tk[i], tv[i])
+    out = torch.empty((L, per, H, wl.dv), device=dev)
+
+    def token(i):
+        for l, st in enumerate(layers):
+            st.step(tq[i, l], tk[i, l], tv[i, l], out[l])
+
+    for i in range(3):
+        token(i % T)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(T):
+            token(i)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    for st in layers:
+        st.close()
+    ms = e0.elapsed_time(e1) / (reps * T)
+    return {"workload": ("batch64 as 28 per-layer launches per token (512 groups each), "
+                         "replayed from a CUDA graph"),
+            "tokens": reps * T, "ms_per_token": ms,
+            "group_steps_per_s": L * per / (ms / 1e3), "launches_per_token": L}
 
 
 def run_layers(args, wl):
@@ -672,6 +777,8 @@ def main():
                     help="distinct decode-token batches kept in HBM (cycled)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the long-context and per-layer graph figures")
     ap.add_argument("--ref-groups", type=int, default=3,
                     help="oracle groups per host core in --impl reference")
     ap.add_argument("--ref-budget", type=float, default=60.0,
