@@ -94,6 +94,53 @@ __device__ __forceinline__ void comp_axpy(float hi, float lo, float r, float x, 
   nlo = t - (nhi - s);
 }
 
+// ---- double-float arithmetic (unevaluated pairs hi + lo of f32) for the
+// sums that need more than f32: GB300's f32 pipe is tens of times faster
+// than its f64 pipe.  df_two_sum is Knuth's exact sum, df_fast_two_sum
+// Dekker's (|a| >= |b|), df_mul the product of two pairs by FMA.
+__device__ __forceinline__ void df_two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float z = s - a;
+  e = (a - (s - z)) + (b - z);
+}
+__device__ __forceinline__ void df_fast_two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  e = b - (s - a);
+}
+__device__ __forceinline__ void df_mul(float ah, float al, float bh, float bl, float& ph,
+                                       float& pl) {
+  const float p = ah * bh;
+  float e = fmaf(ah, bh, -p);
+  e = fmaf(ah, bl, e);
+  e = fmaf(al, bh, e);
+  df_fast_two_sum(p, e, ph, pl);
+}
+__device__ __forceinline__ void df_add(float ah, float al, float bh, float bl, float& sh,
+                                       float& sl) {
+  float s, e;
+  df_two_sum(ah, bh, s, e);
+  e += al + bl;
+  df_fast_two_sum(s, e, sh, sl);
+}
+// e^{a + b - c} for f32 a, b, c, without rounding the exponent: the
+// exponent is formed exactly as a pair (xh, xl) and e^{xh + xl} taken as
+// expf(xh) (1 + xl), |xl| <= ulp(xh) / 2 (the second-order term is below
+// 2^-48).  Returns the value as a pair (hi, lo); only expf's own error
+// remains.  a + b may be -INF (no key absorbed yet): then the result is 0.
+__device__ __forceinline__ void exp_sum_pair(float a, float b, float c, float& hi, float& lo) {
+  float s1, e1, s2, e2, xh, xl;
+  df_two_sum(a, b, s1, e1);
+  df_two_sum(s1, -c, s2, e2);
+  if (!isfinite(s2)) {  // -INF: nothing absorbed (the error terms are NaN)
+    hi = expf(s2);
+    lo = 0.f;
+    return;
+  }
+  df_fast_two_sum(s2, e1 + e2, xh, xl);
+  hi = expf(xh);
+  lo = hi * xl;
+}
+
 // Kahan's compensated update of the running sum hi + lo by one term x * y,
 // after an optional rescale by r: lo carries the rounding error of the
 // running sum (recovered by Fast2Sum), so many steps drift no more than a
@@ -232,6 +279,37 @@ __device__ __forceinline__ float dot2_x4(const float* x, const float* y, int ys,
   const float z = t - s0;
   const float e = (s0 - (t - z)) + (s1 - z);
   return t + ((c0 + c1) + e);
+}
+// dot2_x4 with the result kept as a normalised pair (hi is dot2_x4's value).
+__device__ __forceinline__ void dot2_x4_pair(const float* x, const float* y, int ys, int n,
+                                             float& hi, float& lo) {
+  float s0 = 0.f, c0 = 0.f, s1 = 0.f, c1 = 0.f;
+  auto term = [](float& sv, float& cv, float xa, float ya) {
+    const float h = xa * ya;
+    const float r = fmaf(xa, ya, -h);
+    const float t = sv + h;
+    const float z = t - sv;
+    cv += ((sv - (t - z)) + (h - z)) + r;
+    sv = t;
+  };
+  int a = 0;
+  for (; a + 4 <= n; a += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(x + a);
+    term(s0, c0, xv.x, y[a * ys]);
+    term(s1, c1, xv.y, y[(a + 1) * ys]);
+    term(s0, c0, xv.z, y[(a + 2) * ys]);
+    term(s1, c1, xv.w, y[(a + 3) * ys]);
+  }
+  if (a + 2 <= n) {
+    term(s0, c0, x[a], y[a * ys]);
+    term(s1, c1, x[a + 1], y[(a + 1) * ys]);
+    a += 2;
+  }
+  if (a < n) term(s0, c0, x[a], y[a * ys]);
+  const float t = s0 + s1;
+  const float z = t - s0;
+  const float e = (s0 - (t - z)) + (s1 - z);
+  df_fast_two_sum(t, (c0 + c1) + e, hi, lo);
 }
 
 // bf16 storage of low parts: two values per 32-bit word, round to nearest

@@ -49,34 +49,6 @@ __device__ __forceinline__ void st4(float* p, float4 x) {
   *reinterpret_cast<float4*>(p) = x;
 }
 
-// ---- double-float arithmetic (unevaluated pairs hi + lo of f32) for the
-// parts of the seal that need more than f32: GB300's f32 pipe is tens of
-// times faster than its f64 pipe.
-__device__ __forceinline__ void df_two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float z = s - a;
-  e = (a - (s - z)) + (b - z);
-}
-__device__ __forceinline__ void df_fast_two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  e = b - (s - a);
-}
-__device__ __forceinline__ void df_mul(float ah, float al, float bh, float bl, float& ph,
-                                       float& pl) {
-  const float p = ah * bh;
-  float e = fmaf(ah, bh, -p);
-  e = fmaf(ah, bl, e);
-  e = fmaf(al, bh, e);
-  df_fast_two_sum(p, e, ph, pl);
-}
-__device__ __forceinline__ void df_add(float ah, float al, float bh, float bl, float& sh,
-                                       float& sl) {
-  float s, e;
-  df_two_sum(ah, bh, s, e);
-  e += al + bl;
-  df_fast_two_sum(s, e, sh, sl);
-}
-
 // ---------------------------------------------------------------- 1
 // Knuth's two-sum: a + b = s + e exactly in f32.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {

@@ -46,7 +46,7 @@ __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
 
 // Shared-memory carve-up in floats, identical on host and device.
 struct StepSmem {
-  int q, knew, kev, vnew, vev, sig, fh, lg, rs, es, gs, zs, ms, den, part;
+  int q, knew, kev, vnew, vev, sig, fh, lg, rs, es, gs, zs, ms, gl, zl, den, part;
   int total;
   int nrp, mp;
   __host__ __device__ StepSmem(int ht, int d, int dv, int near, int m) {
@@ -66,6 +66,8 @@ struct StepSmem {
     gs = o;   o += ht * mp;
     zs = o;   o += ht * mp;
     ms = o;   o += ht * mp;
+    gl = o;   o += ht * mp;  // low parts: u, then g (the far denominator's pairs)
+    zl = o;   o += ht * mp;  // low part of Z^
     den = o;  o += round4(ht);
     part = o; o += kWarps * ht * kColTile;
     total = o;
@@ -119,6 +121,8 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
   float* es = sm + L.es;
   float* gs = sm + L.gs;
   float* zs = sm + L.zs;
+  float* gls = sm + L.gl;
+  float* zls = sm + L.zl;
   float* ms = sm + L.ms;
   float* den = sm + L.den;
   float* part = sm + L.part;
@@ -214,6 +218,8 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
       float* hfh = fh + hh * L.mp;
       float* hgs = gs + hh * L.mp;
       float* hzs = zs + hh * L.mp;
+      float* hgl = gls + hh * L.mp;
+      float* hzl = zls + hh * L.mp;
       float* hms = ms + hh * L.mp;
       float* hsig = sig + hh * L.nrp;
       const int32_t fl = s.far_len[hb];
@@ -235,7 +241,8 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
         }
         rs[hh * L.mp + i] = r;
         es[hh * L.mp + i] = e;
-        hzs[i] = zn + zln;
+        hzs[i] = zn;  // Z^ as its pair, for the far denominator
+        hzl[i] = zln;
         hms[i] = mn;
       }
       const int32_t fl_new = fl + (full ? 1 : 0);
@@ -255,19 +262,32 @@ step_kernel(DevState s, int64_t g0, const float* __restrict__ q,
         const float* M = s.mu + hb * m * (int64_t)m;
         float cm = -INFINITY;
         for (int b = lane; b < m_eff; b += 32) {
-          float u = dot2_x4(hfh, M + b, m, m_eff);
-          if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
-          hgs[b] = u;
+          float uh, ul;
+          dot2_x4_pair(hfh, M + b, m, m_eff, uh, ul);
+          if (s.rect == NYS_RECT_FM && uh < 0.f) uh = ul = 0.f;
+          hgs[b] = uh;
+          hgl[b] = ul;
           cm = fmaxf(cm, f + hms[b]);
         }
         c_all = fmaxf(c, warp_max(cm));
-        float acc = 0.f;
+        // The far denominator in double-float (its terms cancel; see the
+        // fast kernel): u as a pair, the exponent unrounded, Z^ as a pair.
+        float dh = 0.f, dl = 0.f;
         for (int b = lane; b < m_eff; b += 32) {
-          const float gb = hgs[b] * expf(f + hms[b] - c_all);
-          hgs[b] = gb;
-          acc = fmaf(gb, hzs[b], acc);
+          float eh, el, gh, glo, th, tl;
+          exp_sum_pair(f, hms[b], c_all, eh, el);
+          df_mul(hgs[b], hgl[b], eh, el, gh, glo);
+          hgs[b] = gh;
+          df_mul(gh, glo, hzs[b], hzl[b], th, tl);
+          df_add(dh, dl, th, tl, dh, dl);
         }
-        far_den = warp_sum(acc);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, dh, o);
+          const float ol = __shfl_xor_sync(0xffffffffu, dl, o);
+          df_add(dh, dl, oh, ol, dh, dl);
+        }
+        far_den = dh + dl;
         if (!(far_den >= 0.f)) {
           far_den = 0.f;
           for (int b = lane; b < m_eff; b += 32) hgs[b] = 0.f;

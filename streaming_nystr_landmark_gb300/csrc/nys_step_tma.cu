@@ -594,7 +594,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           s.z_hat[hb * m + i] = zn;
           s.z_lo[hb * m + i] = zln;
         }
-        hrc[i] = make_float4(r, e, 0.f, zn + zln);
+        // Z^ stays a pair for the far denominator (step (4)): hi in the
+        // rescale record, lo in place of the old lo (no one reads it again).
+        hrc[i] = make_float4(r, e, 0.f, zn);
+        xzlo[hh * m + i] = zln;
         hms[i] = mn;
         mx_m = fmaxf(mx_m, mn);
       }
@@ -613,7 +616,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       c_all = has_far ? fmaxf(cmax, f + mx_m) : cmax;
       if (has_far)
         for (int a = lane; a < m_eff; a += 32) hfh[a] = expf(hfh[a] - f);
-      // (3) Near weights on the joint scale.
+      // (3) Near weights on the joint scale (positive terms: f32 suffices).
       for (int j = lane; j < nnear; j += 32) {
         const float p = expf(hsig[j] - c_all);
         pT[j * HT + hh] = p;
@@ -630,25 +633,39 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
         float* hfh = fh + hh * P.mp;
         float* hms = ms + hh * P.mp;
         // (4) Far mix u = F^ M (rectified), weights g_b on the joint scale,
-        //     far denominator; both sums reduced together.
-        float acc = 0.f;
+        //     far denominator.  The far denominator sum_b g_b Z^_b cancels:
+        //     where u has mixed signs its terms can be thousands of times
+        //     the result, so it is carried in double-float: u as its Dot2
+        //     pair, g_b with its exponent f + m_b - c_all unrounded, Z^ as
+        //     the stored pair, the sum compensated across the warp.  The far
+        //     numerator takes g_b rounded to f32.
+        float dh = 0.f, dl = 0.f;
         if (has_far) {
           __syncwarp();
           // This head's m x m block of M, inside the current M stage.
           const float* Mh = reinterpret_cast<const float*>(stage_ptr(ci)) +
                             (size_t)(hh - h_lo) * m * m;
           for (int b = lane; b < m_eff; b += 32) {
-            float u = dot2_x4(hfh, Mh + b, m, m_eff);
-            if (s.rect == NYS_RECT_FM) u = fmaxf(u, 0.f);
-            const float gb = u * expf(f + hms[b] - c_all);
-            hrc[b].z = gb;
-            acc = fmaf(gb, hrc[b].w, acc);
+            float uh, ul, eh, el, gh, gl, th, tl;
+            dot2_x4_pair(hfh, Mh + b, m, m_eff, uh, ul);
+            if (s.rect == NYS_RECT_FM && uh < 0.f) uh = ul = 0.f;
+            exp_sum_pair(f, hms[b], c_all, eh, el);
+            df_mul(uh, ul, eh, el, gh, gl);
+            hrc[b].z = gh;
+            df_mul(gh, gl, hrc[b].w, xzlo[hh * m + b], th, tl);
+            df_add(dh, dl, th, tl, dh, dl);
           }
         } else {
           for (int b = lane; b < m_eff; b += 32) hrc[b].z = 0.f;
         }
-        warp_sum2(acc, psum);
-        float far_den = has_far ? acc : 0.f;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, dh, o);
+          const float ol = __shfl_xor_sync(0xffffffffu, dl, o);
+          psum += __shfl_xor_sync(0xffffffffu, psum, o);
+          df_add(dh, dl, oh, ol, dh, dl);
+        }
+        float far_den = has_far ? dh + dl : 0.f;
         // Guard: a negative (or NaN) far denominator drops the far field.
         if (has_far && !(far_den >= 0.f)) {
           far_den = 0.f;

@@ -38,12 +38,21 @@ GUARD_BAND = 1e-5
 UNDERFLOW_GAP = 80.0
 
 
+def oracle_workers():
+    """Oracle worker processes for a full-size run: the host's cores but two."""
+    import os
+    return max(1, min(16, (os.cpu_count() or 2) - 2))
+
+
 def row_err(got, ref):
     return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
 
 
 class ParityRun:
-    def __init__(self, wl, sample, device, n_groups=None, host_all=None):
+    """workers > 0: the sampled groups' oracles run in that many spawned
+    processes (oracle_pool.OraclePool), stepped while the GPU steps."""
+
+    def __init__(self, wl, sample, device, n_groups=None, host_all=None, workers=0):
         import torch
         from streaming_nystr_landmark_gb300.nys import NystromStates
         self.torch = torch
@@ -59,14 +68,24 @@ class ParityRun:
         self.flagged = 0
         self.checked = 0
         self.worst = 0.0
+        self.worst_at = None  # (group, token, head, kappa, margin, near_gap)
+        self.workers = workers
+        self.pool = None
+        self.oracles = []
         self.fill = None if self.host_all else DeviceFill(
             wl.with_(seqs=1, layers=1, kv_groups=self.G), device)
 
     # ------------------------------------------------------------ seal
     def seal(self):
         torch, wl, G = self.torch, self.wl, self.G
-        qh, kh, vh, self.gens = host_prompt_batch(wl, self.sample)
+        if self.workers:
+            from oracle_pool import OraclePool
+            # The workers draw the sampled prompts, hand them over, and seal
+            # their oracles while this process seals the GPU.
+            self.pool = OraclePool(wl, self.sample, self.workers, GUARD_BAND, UNDERFLOW_GAP,
+                                   send_prompts=not self.host_all)
         if self.host_all:
+            qh, kh, vh, self.gens = host_prompt_batch(wl, self.sample)
             q = torch.from_numpy(qh).to(self.dev)
             k = torch.from_numpy(kh).to(self.dev)
             v = torch.from_numpy(vh).to(self.dev)
@@ -75,24 +94,47 @@ class ParityRun:
             k = torch.empty((G, wl.t, wl.d), device=self.dev)
             v = torch.empty((G, wl.t, wl.dv), device=self.dev)
             self.fill.prompt_into(q, k, v)
-            idx = torch.tensor(self.sample, device=self.dev)
-            q[idx] = torch.from_numpy(qh).to(self.dev)
-            k[idx] = torch.from_numpy(kh).to(self.dev)
-            v[idx] = torch.from_numpy(vh).to(self.dev)
+            # Host prompts of the sampled groups, a few at a time (a long
+            # prompt is ~0.2 GB); the oracles below, if local, get theirs
+            # regenerated from the same streams.
+            if self.pool is not None:
+                self.gens = []
+                for g, qh, kh, vh, gi in self.pool.prompts():
+                    q[g] = torch.from_numpy(qh).to(self.dev)
+                    k[g] = torch.from_numpy(kh).to(self.dev)
+                    v[g] = torch.from_numpy(vh).to(self.dev)
+                    self.gens.append(gi)
+            else:
+                self.gens = []
+                for c0 in range(0, len(self.sample), 4):
+                    part = self.sample[c0:c0 + 4]
+                    qh, kh, vh, gens = host_prompt_batch(wl, part)
+                    idx = torch.tensor(part, device=self.dev)
+                    q[idx] = torch.from_numpy(qh).to(self.dev)
+                    k[idx] = torch.from_numpy(kh).to(self.dev)
+                    v[idx] = torch.from_numpy(vh).to(self.dev)
+                    self.gens += gens
         self.st.seal(q, k, v)
         torch.cuda.synchronize(self.dev)
         del q, k, v
-        self.oracles = []
-        for i, g in enumerate(self.sample):
-            o = NystromOracle(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.rect)
-            o.prefill(qh[i], kh[i], vh[i])
-            self.oracles.append(o)
+        if self.pool is not None:
+            self.pool.ready()
+        else:
+            self.oracles = []
+            for g in self.sample:
+                qh, kh, vh, _ = host_prompt_batch(wl, [g])
+                o = NystromOracle(wl.m, wl.w, wl.sink, wl.heads_per_kv, wl.rect)
+                o.prefill(qh[0], kh[0], vh[0])
+                self.oracles.append(o)
         self.n_steps = 0
 
     # ------------------------------------------------------------ state
     def check_state(self, far_tol=FAR_TOL):
         """Compare every sampled group's device state with its oracle."""
         regs = read_state(self.st)
+        if self.pool is not None:
+            self.pool.compare_state(regs, far_tol)
+            return
         for o, g in zip(self.oracles, self.sample):
             compare_group_state(regs, g, o, far_tol)
 
@@ -115,10 +157,27 @@ class ParityRun:
             q[idx] = torch.from_numpy(qh).to(self.dev)
             k[idx] = torch.from_numpy(kh).to(self.dev)
             v[idx] = torch.from_numpy(vh).to(self.dev)
+        if self.pool is not None:
+            self.pool.start_step(n)  # the oracles step while the GPU does
         out = torch.empty((G, wl.heads_per_kv, wl.dv), device=self.dev)
         self.st.step(q, k, v, out)
         got = out[torch.tensor(self.sample, device=self.dev)].cpu().numpy()
         self.n_steps += 1
+        if self.pool is not None:
+            refs, flags, diag = self.pool.finish_step()
+            for i in range(len(self.sample)):
+                for h in range(wl.heads_per_kv):
+                    self.checked += 1
+                    if flags[i, h]:
+                        self.flagged += 1
+                        assert np.all(np.isfinite(got[i, h]))
+                        continue
+                    err = row_err(got[i, h].astype(np.float64), refs[i, h])
+                    if err > self.worst:
+                        self.worst = err
+                        self.worst_at = (self.sample[i], n, h, *diag[i, h])
+                    assert err <= OUT_TOL, (self.sample[i], h, n, err, tuple(diag[i, h]))
+            return out
         for i, o in enumerate(self.oracles):
             ref = o.step(qh[i], kh[i], vh[i])
             for h in range(wl.heads_per_kv):
@@ -129,7 +188,9 @@ class ParityRun:
                     self.flagged += 1
                     assert np.all(np.isfinite(got[i, h]))
                     continue
-                self.worst = max(self.worst, err)
+                if err > self.worst:
+                    self.worst = err
+                    self.worst_at = (self.sample[i], n, h, dg.kappa, dg.margin, dg.near_gap)
                 assert err <= OUT_TOL, (self.sample[i], h, n, err)
         return out
 
@@ -146,6 +207,9 @@ class ParityRun:
         assert np.all(ints[:, 5] == 0), "a decode kernel reported a timed-out wait"
 
     def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool = None
         self.st.close()
 
 
