@@ -213,6 +213,12 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream (launch_tma_ht): everything above touches only this CTA's shared
+  // memory, so it may overlap that kernel's tail; nothing global is read
+  // before the previous kernel has completed and its writes are visible.
+  // (Without that launch attribute this returns at once.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ============================================================ producer
   if (warp == kCWarps) {
@@ -384,6 +390,10 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
 
   for (int64_t gi = blockIdx.x; gi < n; gi += gridDim.x, nbuf ^= 1) {
     const int64_t g = g0 + gi;
+    // This CTA's last group: the next kernel on the stream may be scheduled
+    // once every CTA has got here (it still waits for this grid to finish
+    // before it reads anything).
+    if (gi + gridDim.x >= n && tid == 0) asm volatile("griddepcontrol.launch_dependents;");
     float* const xknew = xknew2 + nbuf * d;
     float* const xvnew = xvnew2 + nbuf * dv;
     // far_len of the head this warp owns in the per-head phase; loaded now so
@@ -891,22 +901,30 @@ cudaError_t launch_tma_ht(const DevState& s, const TmaPlan& P, int64_t g0, int64
   const int64_t slots = (int64_t)sms * P.ctas_per_sm;
   const int64_t per = (n + slots - 1) / slots;  // groups per CTA
   const int64_t grid = per <= 4 ? (n + per - 1) / per : slots;
+  // Programmatic dependent launch: this grid's CTAs may be scheduled while
+  // the previous kernel on the stream drains (their prologue then overlaps
+  // its tail); the kernel waits for that kernel's completion before its
+  // first global read (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreadsTma);
+  cfg.dynamicSmemBytes = P.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if constexpr (HT <= 2) {
     if (s.d == 128) {
       cudaError_t e = ensure_smem<step_tma_kernel<HT, 128>>(P.smem_bytes);
       if (e != cudaSuccess) return e;
-      step_tma_kernel<HT, 128><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
-          s, P, g0, n, q, k, v, out);
-      return cudaGetLastError();
+      return cudaLaunchKernelEx(&cfg, step_tma_kernel<HT, 128>, s, P, g0, n, q, k, v, out);
     }
   }
-  {
-    cudaError_t e = ensure_smem<step_tma_kernel<HT, 0>>(P.smem_bytes);
-    if (e != cudaSuccess) return e;
-    step_tma_kernel<HT, 0><<<(unsigned)grid, kThreadsTma, P.smem_bytes, stream>>>(
-        s, P, g0, n, q, k, v, out);
-  }
-  return cudaGetLastError();
+  cudaError_t e = ensure_smem<step_tma_kernel<HT, 0>>(P.smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, step_tma_kernel<HT, 0>, s, P, g0, n, q, k, v, out);
 }
 
 }  // namespace
