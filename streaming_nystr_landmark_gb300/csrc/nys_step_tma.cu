@@ -469,7 +469,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           const bool valid = lr < nrow;
           const int vr = r0 + lr;
           if (valid) {
-            const float* row = stage + (size_t)lr * 128;
+            const float* row = stage + lr * 128;
             if (vr - ns == slot && vr >= ns) row = xknew;
             const float4 a0 = ld4(row + 4 * kgl), a1 = ld4(row + 4 * (kgl + 8));
             const float4 a2 = ld4(row + 4 * (kgl + 16)), a3 = ld4(row + 4 * (kgl + 24));
@@ -524,7 +524,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           const int lr = base + warp * kRR + u;
           if (lr < kend && ck) {
             const int vr = r0 + lr;
-            const float* row = (vr - ns == slot && vr >= ns) ? xknew : stage + (size_t)lr * d;
+            const float* row = (vr - ns == slot && vr >= ns) ? xknew : stage + lr * d;
             const float4 a = ld4(row + 4 * lane);
 #pragma unroll
             for (int hh = 0; hh < HT; ++hh) x[u * HT + hh] = dot4(a, qr[hh]);
@@ -549,7 +549,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
 #pragma unroll
         for (int u = 0; u < kQRows; ++u) {
           const int lr = base + u;
-          x[u] = (lr < nrow && ck) ? dot4(ld4(stage + (size_t)lr * d + 4 * lane), kev4) : 0.f;
+          x[u] = (lr < nrow && ck) ? dot4(ld4(stage + (lr * d + 4 * lane)), kev4) : 0.f;
         }
         const float tot = reduce_multi<kQRows>(x, lane);
         if (reduce_writer<kQRows>(lane)) {
@@ -703,7 +703,7 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
       for (int lr = warp; lr < nrow; lr += kCWarps) {
         const int j = r0 + lr;  // near row: sinks first, then window slots
         if (j < nnear && cv) {
-          const float* row = (j - ns == slot) ? xvnew : stage + (size_t)lr * dv;
+          const float* row = (j - ns == slot) ? xvnew : stage + lr * dv;
           const float4 a = ld4(row + 4 * lane);
           // This row's weight for every head (slots past H hold stale values
           // and feed accumulators that are never written out).
@@ -792,15 +792,15 @@ step_tma_kernel(DevState s, TmaPlan P, int64_t g0, int64_t n, const float* __res
           }
         }
         if (b < m_eff && cv) {
-          float4 x = ld4(hi_rows + (size_t)lr * dv + 4 * lane);
-          const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (size_t)lr * dv + 4 * lane);
+          float4 x = ld4(hi_rows + (lr * dv + 4 * lane));
+          const uint2 lr2 = *reinterpret_cast<const uint2*>(lo_rows + (lr * dv + 4 * lane));
           float4 lo = make_float4(bf16_lo(lr2.x), bf16_hi(lr2.x), bf16_lo(lr2.y), bf16_hi(lr2.y));
           const float4 cf = rc[h * P.mp + b];  // {r, e, g, Z^}
           if (full) {
             // Compensated far update (Kahan form), written back in place:
             // the group's T^ rows are h * m + b = r0 + lr.
             kahan_axpy4(x, lo, cf.x, cf.y, ve);
-            const size_t ro = (size_t)(r0 + lr) * dv;
+            const int ro = (r0 + lr) * dv;  // < H m dv <= 2^16
             st4(t_hi_g + ro, x);
             uint2 lw;
             lw.x = pack_bf16x2(lo.x, lo.y);
